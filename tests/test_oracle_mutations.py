@@ -1,0 +1,195 @@
+"""Mutation checks of the oracle pins: each plausible mistake, planted in the oracle on
+the CPU, must make at least one pin fail. This shows the pins constrain every part of
+the oracle rather than restating it."""
+import numpy as np
+import pytest
+
+import oracle.dflash_ref as R
+import test_oracle_math as M
+import test_oracle_model as MM
+import test_oracle_verify as V
+from golden_io import load_verify_cases
+
+
+def _rope_wrong_sign(x, pos, theta):
+    d = x.shape[-1]; h = d // 2
+    ang = np.outer(np.asarray(pos, dtype=np.float64), R.rope_inv_freq(d, theta))
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+
+
+def _rope_interleaved(x, pos, theta):
+    d = x.shape[-1]
+    ang = np.outer(np.asarray(pos, dtype=np.float64), R.rope_inv_freq(d, theta))
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * c - x2 * s
+    out[..., 1::2] = x2 * c + x1 * s
+    return out
+
+
+def _rope_freq_exponent_d(x, pos, theta):   # theta^(-j/d) instead of theta^(-2j/d)
+    d = x.shape[-1]; h = d // 2
+    j = np.arange(h)
+    ang = np.outer(np.asarray(pos, dtype=np.float64), theta ** (-j / d))
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :h], x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def _rms_no_gain(x, g, eps):
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _rms_eps_outside(x, g, eps):
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * g
+
+
+def _gqa_modulo(q, keys, vals):
+    B, nq, d = q.shape
+    nkv = keys.shape[1]
+    out = np.empty_like(q)
+    for h in range(nq):
+        g = h % nkv
+        s = (q[:, h, :] @ keys[:, g, :].T) / np.sqrt(d)
+        out[:, h, :] = R.softmax(s) @ vals[:, g, :]
+    return out
+
+
+def _causal(q, keys, vals):
+    B, nq, d = q.shape
+    S, nkv = keys.shape[0], keys.shape[1]
+    out = np.empty_like(q)
+    N = S - B
+    for h in range(nq):
+        g = h // (nq // nkv)
+        s = (q[:, h, :] @ keys[:, g, :].T) / np.sqrt(d)
+        for i in range(B):
+            s[i, N + i + 1:] = -np.inf
+        out[:, h, :] = R.softmax(s) @ vals[:, g, :]
+    return out
+
+
+def _no_scale(q, keys, vals):
+    B, nq, d = q.shape
+    nkv = keys.shape[1]
+    out = np.empty_like(q)
+    for h in range(nq):
+        g = h // (nq // nkv)
+        out[:, h, :] = R.softmax(q[:, h, :] @ keys[:, g, :].T) @ vals[:, g, :]
+    return out
+
+
+def _silu_wrong(x):
+    return x / (1.0 + np.exp(x))
+
+
+def _verify_off_by_one(T, d):
+    r = _orig_verify(T, d)
+    t = max(1, r.accept_len - 1) if r.accept_len == len(T) else r.accept_len
+    return R.VerifyResult(t, r.committed[:t], int(r.committed[t - 1]), r.target_argmax)
+
+
+def _verify_highest_tie(T, d):
+    g = T.shape[1] - 1 - np.argmax(np.asarray(T)[:, ::-1], axis=-1)
+    j = 0
+    while j < len(g) - 1 and int(d[j]) == int(g[j]):
+        j += 1
+    return R.VerifyResult(j + 1, g[: j + 1], int(g[j]), g)
+
+
+def _verify_skip_mismatch(T, d):   # counts all matching slots instead of the leading run
+    g = np.argmax(T, axis=-1)
+    j = int(sum(int(d[i]) == int(g[i]) for i in range(len(g) - 1)))
+    return R.VerifyResult(j + 1, g[: j + 1], int(g[j]), g)
+
+
+_orig_verify = R.verify_greedy
+_orig_ctx = R.Oracle.context_feature
+_orig_draft = R.Oracle.draft
+
+
+def _ctx_taps_reversed(self, hidden_bits):
+    return _orig_ctx(self, np.ascontiguousarray(hidden_bits[::-1]))
+
+
+def _ctx_no_norm(self, hidden_bits):
+    hid = R.bf16_to_float(hidden_bits, self.dtype)
+    X = np.concatenate([hid[j] for j in range(hid.shape[0])], axis=-1)
+    return (X @ self.W("w_fc").T) * self.W("g_ctx")
+
+
+MUTATIONS = {
+    "rope_sign": ("apply_rope", _rope_wrong_sign),
+    "rope_interleaved_pairs": ("apply_rope", _rope_interleaved),
+    "rope_freq_exponent": ("apply_rope", _rope_freq_exponent_d),
+    "rms_no_gain": ("rms_norm", _rms_no_gain),
+    "rms_eps_outside_sqrt": ("rms_norm", _rms_eps_outside),
+    "gqa_modulo_mapping": ("gqa_attention", _gqa_modulo),
+    "causal_mask": ("gqa_attention", _causal),
+    "no_softmax_scale": ("gqa_attention", _no_scale),
+    "silu_sign": ("silu", _silu_wrong),
+    "verify_off_by_one": ("verify_greedy", _verify_off_by_one),
+    "verify_tie_highest": ("verify_greedy", _verify_highest_tie),
+    "verify_skips_mismatch": ("verify_greedy", _verify_skip_mismatch),
+    "fc_taps_reversed": ("Oracle.context_feature", _ctx_taps_reversed),
+    "fc_missing_rmsnorm": ("Oracle.context_feature", _ctx_no_norm),
+}
+
+
+def _all_pins(tiny):
+    """Run every pin; return the names of those that fail."""
+    failed = []
+    checks = {
+        "rms_closed": M.test_rmsnorm_closed_form,
+        "rms_eps": M.test_rmsnorm_eps_and_scale,
+        "rope_first_pair": M.test_rope_first_pair_closed_form,
+        "rope_complex": lambda: M.test_rope_matches_complex_rotation(64, 1e6),
+        "attn_mha": M.test_attention_mha_matches_sdpa,
+        "attn_gqa": M.test_attention_gqa_head_mapping_matches_sdpa,
+        "attn_bidir": M.test_attention_is_bidirectional,
+        "silu": M.test_silu_closed_forms,
+        "verify_golden": lambda: [V.test_hand_worked_cases(c) for c in load_verify_cases()],
+        "verify_masks": lambda: V.test_all_agreement_masks(4),
+        "verify_lossless": V.test_lossless_committed_equal_target_greedy,
+        "inject_naive": lambda: MM.test_injection_matches_naive(tiny),
+        "draft_naive": lambda: MM.test_draft_steps_match_naive_recomputation(tiny),
+    }
+    for name, fn in checks.items():
+        try:
+            fn()
+        except Exception:
+            failed.append(name)
+    return failed
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return _make_tiny()
+
+
+def _make_tiny():
+    from synth import W_TINY
+    from synth import inputs as I
+    s = W_TINY.shape
+    return s, I.make_weights(s, MM.SEED).bits(), I.bf16_bits(I.make_hidden(s, 160, MM.SEED))
+
+
+def test_unmutated_oracle_passes_every_pin(tiny):
+    assert _all_pins(tiny) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tiny, monkeypatch):
+    target, fn = MUTATIONS[name]
+    if target.startswith("Oracle."):
+        monkeypatch.setattr(R.Oracle, target.split(".", 1)[1], fn)
+    else:
+        monkeypatch.setattr(R, target, fn)
+        for mod in (M, V):                       # modules that imported the name directly
+            if hasattr(mod, target):
+                monkeypatch.setattr(mod, target, fn)
+    failed = _all_pins(tiny)
+    assert failed, f"mutation {name} survived every pin"
