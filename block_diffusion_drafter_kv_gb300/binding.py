@@ -1,0 +1,194 @@
+"""ctypes binding of libdflash.so (include/dflash.h): argument marshalling only.
+
+Every step of the draft-and-verify path runs in the library's CUDA kernels. PyTorch
+supplies device memory and the current stream. If the shared library is missing the
+import of `lib()` raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int32, c_size_t, c_void_p
+from typing import Optional
+
+from .build import LIB_PATH
+
+DFLASH_OK = 0
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: "capacity exceeded",
+          -4: "CUDA error", -5: "state not bound"}
+DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4
+
+
+class DflashConfig(ctypes.Structure):
+    _fields_ = [("hidden", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
+                ("n_layers", c_int32), ("intermediate", c_int32), ("vocab", c_int32), ("n_taps", c_int32),
+                ("target_hidden", c_int32), ("rope_theta", c_float), ("rms_eps", c_float),
+                ("max_block", c_int32), ("max_batch", c_int32), ("kv_capacity", c_int32)]
+
+
+class DflashLayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "g_attn", "g_mlp")]
+
+
+class DflashWeights(ctypes.Structure):
+    _fields_ = [("w_fc", c_void_p), ("g_ctx", c_void_p), ("embed", c_void_p), ("mask_emb", c_void_p),
+                ("g_final", c_void_p), ("lm_head", c_void_p), ("layers", POINTER(DflashLayerWeights))]
+
+
+# name -> (restype, argtypes); mirrors include/dflash.h
+SIGNATURES = {
+    "dflash_config_check": (c_int32, [POINTER(DflashConfig)]),
+    "dflash_workspace_size": (c_size_t, [POINTER(DflashConfig)]),
+    "dflash_create": (c_int32, [POINTER(DflashConfig), POINTER(DflashWeights), POINTER(c_void_p)]),
+    "dflash_destroy": (c_int32, [c_void_p]),
+    "dflash_bind_state": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t]),
+    "dflash_inject_ctx": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p]),
+    "dflash_draft_block": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dflash_verify_greedy": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
+                                       c_void_p]),
+    "dflash_linear_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
+                                     c_void_p]),
+    "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32]),
+    "dflash_last_launch_count": (c_int32, [c_void_p]),
+    "dflash_status_string": (ctypes.c_char_p, [c_int32]),
+    "dflash_synth_plant": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
+                                     c_float, c_void_p, c_void_p]),
+    "dflash_synth_unplant": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
+}
+
+_LIB = None
+
+
+def lib(path: Optional[str] = None):
+    """Load libdflash.so (built by `build.build()`); raises if it is absent."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libdflash.so not found at {p}: run block_diffusion_drafter_kv_gb300.build.build()")
+    L = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _LIB = L
+    return L
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+def check(status: int, what: str) -> None:
+    if status != DFLASH_OK:
+        raise DFlashError(status, what)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def make_config(shape, max_block: int, max_batch: int, kv_capacity: int) -> DflashConfig:
+    return DflashConfig(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.n_layers,
+                        shape.intermediate, shape.vocab, shape.n_taps, shape.target_hidden,
+                        float(shape.rope_theta), float(shape.rms_eps), max_block, max_batch, kv_capacity)
+
+
+class Drafter:
+    """One registered drafter plus its caller-owned state (KV caches, lengths, workspace).
+
+    `weights` has the attributes of the input generator's `Weights` (bf16 CUDA tensors)."""
+
+    def __init__(self, shape, weights, max_block: int, max_batch: int, kv_capacity: int):
+        import torch
+        self.L = lib()
+        self.shape = shape
+        self.cfg = make_config(shape, max_block, max_batch, kv_capacity)
+        self.weights = weights  # keep the tensors alive
+        lw = (DflashLayerWeights * shape.n_layers)()
+        for i, w in enumerate(weights.layers):
+            lw[i] = DflashLayerWeights(*[getattr(w, n).data_ptr() for n in
+                                         ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "g_attn", "g_mlp")])
+        self._lw = lw
+        W = DflashWeights(weights.w_fc.data_ptr(), weights.g_ctx.data_ptr(), weights.embed.data_ptr(),
+                          weights.mask_emb.data_ptr(), weights.g_final.data_ptr(), weights.lm_head.data_ptr(),
+                          ctypes.cast(lw, POINTER(DflashLayerWeights)))
+        h = c_void_p()
+        check(self.L.dflash_create(ctypes.byref(self.cfg), ctypes.byref(W), ctypes.byref(h)), "dflash_create")
+        self.h = h
+        dev = weights.w_fc.device
+        s = shape
+        self.k_cache = torch.zeros(s.n_layers, max_batch, kv_capacity, s.n_kv_heads, s.head_dim,
+                                   dtype=torch.bfloat16, device=dev)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.len = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+        self.last_token = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+        nbytes = self.L.dflash_workspace_size(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise DFlashError(-2, "dflash_workspace_size")
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+        base = self.workspace.data_ptr()
+        self._ws_ptr = (base + 255) // 256 * 256
+        check(self.L.dflash_bind_state(self.h, self.k_cache.data_ptr(), self.v_cache.data_ptr(),
+                                       self.len.data_ptr(), self.last_token.data_ptr(), self._ws_ptr, nbytes),
+              "dflash_bind_state")
+
+    # -- the three calls of the step ---------------------------------------------------
+    def inject(self, hidden, rows_per_seq: int, n_new, batch: int, stream=None):
+        check(self.L.dflash_inject_ctx(self.h, hidden.data_ptr(), rows_per_seq, n_new.data_ptr(), batch,
+                                       _stream(stream)), "dflash_inject_ctx")
+
+    def draft(self, batch: int, block: int, drafted, logits=None, x_trace=None, stream=None):
+        check(self.L.dflash_draft_block(self.h, batch, block, _ptr(drafted), _ptr(logits), _ptr(x_trace),
+                                        _stream(stream)), "dflash_draft_block")
+
+    def verify(self, target_logits, drafted, batch: int, block: int, accept_len, committed, stream=None):
+        check(self.L.dflash_verify_greedy(self.h, target_logits.data_ptr(), _ptr(drafted), batch, block,
+                                          accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
+              "dflash_verify_greedy")
+
+    # -- helpers -------------------------------------------------------------------------
+    def linear(self, W, X, Y, stream=None):
+        check(self.L.dflash_linear_bf16(self.h, W.data_ptr(), W.shape[0], W.shape[1], X.data_ptr(), X.shape[0],
+                                        Y.data_ptr(), _stream(stream)), "dflash_linear_bf16")
+
+    def device_error(self, clear: bool = True) -> int:
+        f = c_int32(0)
+        check(self.L.dflash_read_device_error(self.h, ctypes.byref(f), 1 if clear else 0), "dflash_read_device_error")
+        return f.value
+
+    def last_launch_count(self) -> int:
+        return self.L.dflash_last_launch_count(self.h)
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def synth_plant(logits, drafted, masks, n_steps: int, step_counter, batch: int, block: int, bump: float, saved,
+                stream=None):
+    check(lib().dflash_synth_plant(logits.data_ptr(), _ptr(drafted), masks.data_ptr(), n_steps,
+                                   step_counter.data_ptr(), batch, block, logits.shape[-1], bump, saved.data_ptr(),
+                                   _stream(stream)), "dflash_synth_plant")
+
+
+def synth_unplant(logits, step_counter, n_steps: int, batch: int, block: int, saved, stream=None):
+    check(lib().dflash_synth_unplant(logits.data_ptr(), step_counter.data_ptr(), n_steps, batch, block,
+                                     saved.data_ptr(), _stream(stream)), "dflash_synth_unplant")

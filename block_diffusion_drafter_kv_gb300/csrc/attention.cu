@@ -1,0 +1,356 @@
+// Bidirectional block attention of the DFlash drafter (sm_103a).
+//
+// Every slot of the block attends, without a causal mask, to all injected context keys
+// [0, len) and to the block's own B keys [len, len+B) (jansverre.net, "Hva gjør DFlash
+// annerledes enn vanlig spekulativ dekoding?": the masked block is denoised in a single
+// pass; theaistack.guide, "L'idea chiave": the injected K/V live in the draft KV cache).
+// The block's keys were written into the cache at [len, len+B) by the Q/K/V epilogue, so
+// the key range is one contiguous run.
+//
+// Split-KV flash decoding: one thread-block cluster per (sequence, KV head); the CTAs of
+// the cluster split the key range. In a CTA, warp w serves query head g*group + w for all
+// (<= 16) block slots, so the group's query heads share every K/V tile staged in shared
+// memory by TMA. QKᵀ and PV run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate) with an online softmax in registers. The CTAs' partial (max, sum, output)
+// are merged through distributed shared memory in a fixed order, so no partials touch HBM.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+constexpr int KT = 64;       // keys per tile
+constexpr int STAGES = 3;
+
+DEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+DEV void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+DEV uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte address of element (key, d) in a K or V tile: D/64 TMA boxes of 64 keys x 128 bytes,
+// each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
+DEV uint32_t kv_addr(uint32_t base, int key, int d) {
+  const int box = d >> 6, dd = d & 63;
+  return base + box * (KT * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnParams P) {
+  constexpr int TILE_BYTES = KT * D * 2;
+  constexpr int NBOX = D / 64;
+  constexpr int NT_D = D / 8;   // n-tiles over d in the output
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * 2 * TILE_BYTES);
+  uint64_t* empty = full + STAGES;
+  float* s_m = reinterpret_cast<float*>(empty + STAGES);  // [128] per-row running max (log2 units)
+  float* s_l = s_m + 128;                                  // [128] per-row sum
+  float* s_w = s_l + 128;                                  // [128 rows][16] combine weights
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_w + 128 * 16);
+  float* s_o = reinterpret_cast<float*>(smem);             // [rows][D] after the key loop
+
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.y, seq = blockIdx.z;
+  const int S = gridDim.x;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int B = P.B;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nw);
+    }
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&P.kmap);
+    tma_prefetch_desc(&P.vmap);
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  int nkeys = __ldcg(P.len + seq) + B;
+  if (nkeys > P.cap) nkeys = P.cap;
+  const int ntiles = (nkeys + KT - 1) / KT;
+  const int t0 = rank * ntiles / S, t1 = (rank + 1) * ntiles / S;
+  const int n = t1 - t0;
+  const int key_row0 = seq * P.cap;
+
+  // prologue: the first STAGES key tiles (the KV cache is kept in L2 with evict_last)
+  if (threadIdx.x == 0) {
+    const int pre = n < STAGES ? n : STAGES;
+    for (int i = 0; i < pre; ++i) {
+      const int st = i % STAGES;
+      uint8_t* kd = smem + st * 2 * TILE_BYTES;
+      uint8_t* vd = kd + TILE_BYTES;
+      const int row = key_row0 + (t0 + i) * KT;
+      const uint64_t pol = policy_evict_last();
+      mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
+#pragma unroll
+      for (int b = 0; b < NBOX; ++b) {
+        tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
+        tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
+      }
+    }
+  }
+
+  // Q fragments of this warp's head: rows = block slots (>= B are zero).
+  const int nq = P.nq;
+  const int h = g * nw + warp;
+  const int r0 = lane >> 2, kq = (lane & 3) * 2;
+  uint32_t qa[D / 16][4];
+  {
+    const size_t ld = static_cast<size_t>(nq) * D;
+    const __nv_bfloat16* qrow0 = P.q + (static_cast<size_t>(seq) * B + r0) * ld + h * D;
+    const __nv_bfloat16* qrow1 = qrow0 + 8 * ld;
+    const bool v0 = r0 < B, v1 = r0 + 8 < B;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c = kk * 16 + kq;
+      qa[kk][0] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow0 + c)) : 0u;
+      qa[kk][1] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow1 + c)) : 0u;
+      qa[kk][2] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow0 + c + 8)) : 0u;
+      qa[kk][3] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow1 + c + 8)) : 0u;
+    }
+  }
+
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o[NT_D][4];
+#pragma unroll
+  for (int i = 0; i < NT_D; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  for (int i = 0; i < n; ++i) {
+    const int st = i % STAGES;
+    if (!*s_abort && !mbar_wait(&full[st], (i / STAGES) & 1)) {
+      *s_abort = 1;
+      raise_flag(P.err, kDevTimeout);
+    }
+    const uint32_t kb = smem_u32(smem + st * 2 * TILE_BYTES);
+    const uint32_t vb = kb + TILE_BYTES;
+    const int key0 = (t0 + i) * KT;
+
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int mi = lane >> 3;
+        const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
+        const int d = kk * 16 + (mi & 1) * 8;
+        uint32_t b[4];
+        ldsm_x4(kv_addr(kb, key, d), b);
+        mma_bf16_16816(sc[2 * np], qa[kk], b[0], b[1]);
+        mma_bf16_16816(sc[2 * np + 1], qa[kk], b[2], b[3]);
+      }
+    }
+    // scale to log2 units, mask keys past the end, online softmax
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = key0 + j * 8 + kq + (c & 1);
+        const float v = key < nkeys ? sc[j][c] * P.scale_log2 : -INFINITY;
+        sc[j][c] = v;
+        mx[c >> 1] = fmaxf(mx[c >> 1], v);
+      }
+    }
+    float corr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mnew = fmaxf(m_run[r], mx[r]);
+      const float base = mnew == -INFINITY ? 0.f : mnew;
+      corr[r] = exp2f(m_run[r] - base);
+      m_run[r] = mnew;
+      mx[r] = base;
+    }
+    float ls[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float p = exp2f(sc[j][c] - mx[c >> 1]);
+        sc[j][c] = p;
+        ls[c >> 1] += p;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * corr[r] + ls[r];
+#pragma unroll
+    for (int nt = 0; nt < NT_D; ++nt) {
+      o[nt][0] *= corr[0];
+      o[nt][1] *= corr[0];
+      o[nt][2] *= corr[1];
+      o[nt][3] *= corr[1];
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        const int mi = lane >> 3;
+        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
+        const int d = dp * 16 + (mi >> 1) * 8;
+        uint32_t b[4];
+        ldsm_x4_trans(kv_addr(vb, key, d), b);
+        mma_bf16_16816(o[2 * dp], pa, b[0], b[1]);
+        mma_bf16_16816(o[2 * dp + 1], pa, b[2], b[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (threadIdx.x == 0 && i + STAGES < n) {
+      if (!*s_abort && !mbar_wait(&empty[st], (i / STAGES) & 1)) {
+        *s_abort = 1;
+        raise_flag(P.err, kDevTimeout);
+      }
+      if (!*s_abort) {
+        const uint64_t pol = policy_evict_last();
+        uint8_t* kd = smem + st * 2 * TILE_BYTES;
+        uint8_t* vd = kd + TILE_BYTES;
+        const int row = key_row0 + (t0 + i + STAGES) * KT;
+        mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
+#pragma unroll
+        for (int b = 0; b < NBOX; ++b) {
+          tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
+          tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
+        }
+      }
+    }
+  }
+
+  // row sums across the quad
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+  }
+  __syncthreads();  // the ring is free: every issued tile was consumed
+  {
+    const int ra = warp * 16 + r0, rb = ra + 8;
+#pragma unroll
+    for (int nt = 0; nt < NT_D; ++nt) {
+      const int d = nt * 8 + kq;
+      s_o[ra * D + d] = o[nt][0];
+      s_o[ra * D + d + 1] = o[nt][1];
+      s_o[rb * D + d] = o[nt][2];
+      s_o[rb * D + d + 1] = o[nt][3];
+    }
+    if ((lane & 3) == 0) {
+      s_m[ra] = m_run[0];
+      s_m[rb] = m_run[1];
+      s_l[ra] = l_run[0];
+      s_l[rb] = l_run[1];
+    }
+  }
+  cluster_sync();
+
+  // merge: this CTA owns rows [rb0, rb1) of the nw*16 query rows
+  const int R = nw * 16;
+  const int per = (R + S - 1) / S;
+  const int rb0 = rank * per, rb1 = min(R, rb0 + per);
+  for (int rr = rb0 + static_cast<int>(threadIdx.x); rr < rb1; rr += blockDim.x) {
+    float M = -INFINITY;
+    for (int c = 0; c < S; ++c) M = fmaxf(M, ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c)));
+    float den = 0.f;
+    for (int c = 0; c < S; ++c) {
+      const float mc = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c));
+      const float lc = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_l[rr]), c));
+      const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
+      s_w[(rr - rb0) * 16 + c] = w;
+      den += w * lc;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = 0; c < S; ++c) s_w[(rr - rb0) * 16 + c] *= inv;
+  }
+  __syncthreads();
+  const int cnt = (rb1 - rb0) * D;
+  for (int idx = threadIdx.x; idx < cnt; idx += blockDim.x) {
+    const int rr = rb0 + idx / D, d = idx % D;
+    const int w = rr >> 4, slot = rr & 15;
+    if (slot >= B) continue;
+    float acc = 0.f;
+    for (int c = 0; c < S; ++c)
+      acc += s_w[(rr - rb0) * 16 + c] * ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_o[rr * D + d]), c));
+    P.o[(static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d] =
+        __float2bfloat16_rn(acc);
+  }
+  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+template <int D>
+static int attn_smem() {
+  return 1024 + STAGES * 2 * (KT * D * 2) + STAGES * 16 + (128 * 2 + 128 * 16) * 4 + 16;
+}
+
+int attn_set_attributes() {
+  cudaError_t e = cudaSuccess;
+#define DFL_ATTN_ATTR(D)                                                                                   \
+  if (e == cudaSuccess)                                                                                    \
+    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem<D>()); \
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  DFL_ATTN_ATTR(64) DFL_ATTN_ATTR(128)
+#undef DFL_ATTN_ATTR
+  return static_cast<int>(e);
+}
+
+template <int D>
+static int launch_d(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl) {
+  const int group = p.nq / p.nkv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, p.nkv, batch);
+  cfg.blockDim = dim3(32 * group);
+  cfg.dynamicSmemBytes = attn_smem<D>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, attn_kernel<D>, p));
+}
+
+int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl) {
+  if (p.d == 128) return launch_d<128>(p, batch, split, stream, pdl);
+  if (p.d == 64) return launch_d<64>(p, batch, split, stream, pdl);
+  return static_cast<int>(cudaErrorInvalidValue);
+}
+
+}  // namespace dfl

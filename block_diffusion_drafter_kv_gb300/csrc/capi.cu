@@ -1,0 +1,700 @@
+// C ABI of the DFlash draft-and-verify step (declared in include/dflash.h).
+//
+// Host side only: argument checks, the workspace layout, TMA descriptor encoding and the
+// launch sequence of each call. Every step of the computation runs in the kernels of
+// gemv.cu, attention.cu and small.cu.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "dflash.h"
+#include "internal.h"
+
+using namespace dfl;
+
+namespace {
+
+constexpr int kMaxChunks = 64;   // verification chunks per row
+constexpr int kMaxLayersPerKvLaunch = kMaxAMaps / 2;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+struct WsLayout {
+  size_t err, tile_cnt, cta_cnt, seq_cnt, rope_cos, rope_sin, part, best_v, best_i;
+  size_t ss_fc, ss_x, ss_emb, cfeat, x, xg, q, o, act, vpart_v, vpart_i, plant;
+  size_t total;
+  int R;          // draft rows allocated (multiple of 16)
+  int max_tiles;  // tile counters
+};
+
+int max_tiles(const dflash_config& c) {
+  const int d = c.head_dim;
+  int t = ceil_div(c.vocab, 128);
+  t = std::max(t, c.hidden / 128);
+  t = std::max(t, (c.n_heads + 2 * c.n_kv_heads) * d / 128);
+  t = std::max(t, c.intermediate / 64);
+  t = std::max(t, 2 * kMaxLayersPerKvLaunch * c.n_kv_heads * d / 128);
+  return t;
+}
+
+WsLayout layout_of(const dflash_config& c) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1), 256);
+    return o;
+  };
+  const size_t H = c.hidden, d = c.head_dim, nq = c.n_heads, I = c.intermediate;
+  L.R = static_cast<int>(align_up(static_cast<size_t>(c.max_batch) * c.max_block, 16));
+  L.max_tiles = max_tiles(c);
+  const size_t R = L.R;
+  L.err = take(256);
+  L.tile_cnt = take(static_cast<size_t>(L.max_tiles) * 4);
+  L.cta_cnt = take(256);
+  L.seq_cnt = take(static_cast<size_t>(c.max_batch) * 4);
+  L.rope_cos = take(static_cast<size_t>(c.kv_capacity) * (d / 2) * 4);
+  L.rope_sin = take(static_cast<size_t>(c.kv_capacity) * (d / 2) * 4);
+  L.part = take(static_cast<size_t>(2) * kMaxCtas * kMaxPassRows * 128 * 4);
+  L.best_v = take(static_cast<size_t>(kMaxCtas) * kMaxPassRows * 4);
+  L.best_i = take(static_cast<size_t>(kMaxCtas) * kMaxPassRows * 4);
+  L.ss_fc = take((H / 128) * kMaxPassRows * 4);
+  L.ss_x = take((H / 128) * R * 4);
+  L.ss_emb = take(R * 4);
+  L.cfeat = take(static_cast<size_t>(kMaxPassRows) * H * 2);
+  L.x = take(R * H * 4);
+  L.xg = take(R * H * 2);
+  L.q = take(R * nq * d * 2);
+  L.o = take(R * nq * d * 2);
+  L.act = take(R * I * 2);
+  L.vpart_v = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
+  L.vpart_i = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
+  L.total = off;
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 row-major [rows][inner], box 64 (inner) x box_rows, 128-byte swizzle.
+bool enc2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [taps][rows][Ht], box 64 x box_rows x 1.
+bool enc3d_hidden(CUtensorMap* m, const void* base, uint64_t Ht, uint64_t rows, uint64_t taps, uint32_t box_rows) {
+  cuuint64_t dims[3] = {Ht, rows, taps};
+  cuuint64_t strides[2] = {Ht * 2, Ht * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One layer's cache bf16 [rows = max_batch*cap][nkv][d], box 64 (d) x 1 head x 64 keys.
+bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
+  cuuint64_t dims[3] = {d, nkv, rows};
+  cuuint64_t strides[2] = {d * 2, nkv * d * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int nb_index(int nb) { return nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : nb == 8 ? 3 : 4; }
+int nb_for_rows(int rows) {
+  int nb = 1;
+  while (nb * 16 < rows && nb < 16) nb *= 2;
+  return nb;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+struct dflash_handle {
+  dflash_config cfg{};
+  dflash_weights w{};
+  std::vector<dflash_layer_weights> layers;
+  int device = 0;
+  int n_sms = 0;
+  int inject_pass_rows = 16;
+  // weight descriptors
+  CUtensorMap m_fc{}, m_lm{};
+  std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
+  // bound state
+  bool bound = false;
+  __nv_bfloat16* kc = nullptr;
+  __nv_bfloat16* vc = nullptr;
+  int* len = nullptr;
+  int* last_token = nullptr;
+  uint8_t* ws = nullptr;
+  WsLayout L{};
+  CUtensorMap m_xg[5]{}, m_cfeat[5]{}, m_act[5]{}, m_o[5]{};
+  std::vector<CUtensorMap> m_kcache, m_vcache;
+  int last_launches = 0;
+
+  template <typename T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+};
+
+namespace {
+
+void gemv_common(const dflash_handle* h, GemvParams& P) {
+  P.part = h->at<float>(h->L.part);
+  P.tile_cnt = h->at<int>(h->L.tile_cnt);
+  P.cta_cnt = h->at<int>(h->L.cta_cnt);
+  P.err = h->at<int>(h->L.err);
+  P.eps = h->cfg.rms_eps;
+  P.H = h->cfg.hidden;
+  P.n_valid = 0x7fffffff;
+  P.n_out = 0x7fffffff;
+}
+
+int run_gemv(dflash_handle* h, const GemvParams& P, int nb, cudaStream_t st) {
+  const long long U = static_cast<long long>(P.T) * P.KB;
+  const int G = static_cast<int>(std::min<long long>(std::min(h->n_sms, kMaxCtas), U));
+  const int e = launch_gemv(P, nb, G, st, true);
+  ++h->last_launches;
+  return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
+}
+
+#define DFL_TRY(x)                \
+  do {                            \
+    const int _r = (x);           \
+    if (_r != DFLASH_OK) return _r; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int dflash_config_check(const dflash_config* c) {
+  if (!c) return DFLASH_E_INVAL;
+  const int d = c->head_dim;
+  bool ok = c->hidden >= 128 && c->hidden % 128 == 0 && c->n_heads >= 1 && c->n_kv_heads >= 1 &&
+            c->n_heads % c->n_kv_heads == 0 && c->n_heads / c->n_kv_heads <= 8 && (d == 64 || d == 128) &&
+            (c->n_heads * d) % 128 == 0 && (c->n_kv_heads * d) % 128 == 0 && c->n_layers >= 1 &&
+            c->n_layers <= 16 && c->intermediate >= 64 && c->intermediate % 64 == 0 && c->vocab >= 2 &&
+            c->n_taps >= 1 && c->n_taps <= 16 && c->target_hidden >= 64 && c->target_hidden % 64 == 0 &&
+            c->rope_theta > 0.f && c->rms_eps >= 0.f && c->max_block >= 1 && c->max_block <= 16 &&
+            c->max_batch >= 1 && c->max_batch <= 256 && c->kv_capacity >= c->max_block &&
+            static_cast<long long>(c->max_batch) * c->kv_capacity < (1LL << 31) &&
+            ceil_div(c->vocab, 128) <= 65536;
+  return ok ? DFLASH_OK : DFLASH_E_CONFIG;
+}
+
+size_t dflash_workspace_size(const dflash_config* c) {
+  if (dflash_config_check(c) != DFLASH_OK) return 0;
+  return layout_of(*c).total;
+}
+
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out) {
+  if (!cfg || !w || !out) return DFLASH_E_INVAL;
+  DFL_TRY(dflash_config_check(cfg));
+  const void* globals[] = {w->w_fc, w->g_ctx, w->embed, w->mask_emb, w->g_final, w->lm_head};
+  for (const void* p : globals)
+    if (!p || !aligned16(p)) return DFLASH_E_INVAL;
+  if (!w->layers) return DFLASH_E_INVAL;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    const void* ps[] = {lw.wq, lw.wk, lw.wv, lw.wo, lw.w_gate, lw.w_up, lw.w_down, lw.g_attn, lw.g_mlp};
+    for (const void* p : ps)
+      if (!p || !aligned16(p)) return DFLASH_E_INVAL;
+  }
+  if (!get_encoder()) return DFLASH_E_CUDA;
+  auto* h = new dflash_handle();
+  h->cfg = *cfg;
+  h->w = *w;
+  h->layers.assign(w->layers, w->layers + cfg->n_layers);
+  h->w.layers = h->layers.data();
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+      gemv_set_attributes() != 0 || attn_set_attributes() != 0) {
+    delete h;
+    return DFLASH_E_CUDA;
+  }
+  const auto& c = *cfg;
+  const uint64_t H = c.hidden, d = c.head_dim, I = c.intermediate;
+  bool ok = enc2d(&h->m_fc, w->w_fc, static_cast<uint64_t>(c.n_taps) * c.target_hidden, H, 64) &&
+            enc2d(&h->m_lm, w->lm_head, H, c.vocab, 64);
+  const int L = c.n_layers;
+  for (auto* v : {&h->m_wq, &h->m_wk, &h->m_wv, &h->m_wo, &h->m_wg, &h->m_wu, &h->m_wd}) v->resize(L);
+  for (int l = 0; l < L && ok; ++l) {
+    const dflash_layer_weights& lw = h->layers[l];
+    ok = enc2d(&h->m_wq[l], lw.wq, H, c.n_heads * d, 64) && enc2d(&h->m_wk[l], lw.wk, H, c.n_kv_heads * d, 64) &&
+         enc2d(&h->m_wv[l], lw.wv, H, c.n_kv_heads * d, 64) && enc2d(&h->m_wo[l], lw.wo, c.n_heads * d, H, 64) &&
+         enc2d(&h->m_wg[l], lw.w_gate, H, I, 64) && enc2d(&h->m_wu[l], lw.w_up, H, I, 64) &&
+         enc2d(&h->m_wd[l], lw.w_down, I, H, 64);
+  }
+  if (!ok) {
+    delete h;
+    return DFLASH_E_CUDA;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_destroy(dflash_handle* h) {
+  if (!h) return DFLASH_E_INVAL;
+  delete h;
+  return DFLASH_OK;
+}
+
+int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* len, int32_t* last_token,
+                      void* workspace, size_t workspace_bytes) {
+  if (!h || !k_cache || !v_cache || !len || !last_token || !workspace) return DFLASH_E_INVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(k_cache) || !aligned16(v_cache))
+    return DFLASH_E_INVAL;
+  const auto& c = h->cfg;
+  const WsLayout L = layout_of(c);
+  if (workspace_bytes < L.total) return DFLASH_E_CAPACITY;
+  h->kc = static_cast<__nv_bfloat16*>(k_cache);
+  h->vc = static_cast<__nv_bfloat16*>(v_cache);
+  h->len = len;
+  h->last_token = last_token;
+  h->ws = static_cast<uint8_t*>(workspace);
+  h->L = L;
+  if (cudaMemset(workspace, 0, L.total) != cudaSuccess) return DFLASH_E_CUDA;
+  // RoPE tables: angle = pos * theta^(-2j/d), computed in double, stored as fp32.
+  const int half = c.head_dim / 2;
+  std::vector<float> cs(static_cast<size_t>(c.kv_capacity) * half), sn(cs.size());
+  for (int p = 0; p < c.kv_capacity; ++p)
+    for (int j = 0; j < half; ++j) {
+      const double inv = std::pow(static_cast<double>(c.rope_theta), -2.0 * j / c.head_dim);
+      const double a = static_cast<double>(p) * inv;
+      cs[static_cast<size_t>(p) * half + j] = static_cast<float>(std::cos(a));
+      sn[static_cast<size_t>(p) * half + j] = static_cast<float>(std::sin(a));
+    }
+  if (cudaMemcpy(h->ws + L.rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(h->ws + L.rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return DFLASH_E_CUDA;
+  const uint64_t H = c.hidden, d = c.head_dim;
+  bool ok = true;
+  for (int k = 0; k < 5 && ok; ++k) {
+    const uint32_t box = 16u << k;
+    ok = enc2d(&h->m_xg[k], h->ws + L.xg, H, L.R, box) &&
+         enc2d(&h->m_cfeat[k], h->ws + L.cfeat, H, kMaxPassRows, box) &&
+         enc2d(&h->m_act[k], h->ws + L.act, c.intermediate, L.R, box) &&
+         enc2d(&h->m_o[k], h->ws + L.o, c.n_heads * d, L.R, box);
+  }
+  h->m_kcache.resize(c.n_layers);
+  h->m_vcache.resize(c.n_layers);
+  const size_t layer_elems = static_cast<size_t>(c.max_batch) * c.kv_capacity * c.n_kv_heads * d;
+  for (int l = 0; l < c.n_layers && ok; ++l) {
+    const uint64_t rows = static_cast<uint64_t>(c.max_batch) * c.kv_capacity;
+    ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
+         enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, rows);
+  }
+  if (!ok) return DFLASH_E_CUDA;
+  h->bound = true;
+  return DFLASH_OK;
+}
+
+int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq, const int32_t* n_new,
+                      int32_t batch, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  if (!hidden || !n_new || !aligned16(hidden) || rows_per_seq < 1 || batch < 1) return DFLASH_E_INVAL;
+  if (batch > c.max_batch) return DFLASH_E_CAPACITY;
+  const long long total_rows = static_cast<long long>(batch) * rows_per_seq;
+  if (total_rows >= (1LL << 31)) return DFLASH_E_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_launches = 0;
+  const int pass_rows = h->inject_pass_rows;
+  const int nb = pass_rows / 16;
+  const int n_pass = ceil_div(total_rows, pass_rows);
+  CUtensorMap m_hidden;
+  if (!enc3d_hidden(&m_hidden, hidden, c.target_hidden, total_rows, c.n_taps, pass_rows)) return DFLASH_E_CUDA;
+  const int H = c.hidden, d = c.head_dim;
+  const int tkv = c.n_kv_heads * d / 128;
+  for (int p = 0; p < n_pass; ++p) {
+    const int row0 = p * pass_rows;
+    {  // context fusion: F = concat(hidden taps) · Wfcᵀ
+      GemvParams P{};
+      gemv_common(h, P);
+      P.amap[0] = h->m_fc;
+      P.n_amaps = 1;
+      P.tile_start[0] = 0;
+      P.tile_start[1] = H / 128;
+      P.T = H / 128;
+      P.KB = c.n_taps * c.target_hidden / 64;
+      P.bmap = m_hidden;
+      P.b3d = 1;
+      P.b_kb_per_tap = c.target_hidden / 64;
+      P.b_row0 = row0;
+      P.grow0 = row0;
+      P.out_row0 = 0;
+      P.op = OP_FC;
+      P.gain = static_cast<const __nv_bfloat16*>(h->w.g_ctx);
+      P.yb = h->at<__nv_bfloat16>(h->L.cfeat);
+      P.yb_ld = H;
+      P.ss_out = h->at<float>(h->L.ss_fc);
+      P.ss_stride = kMaxPassRows;
+      DFL_TRY(run_gemv(h, P, nb, st));
+    }
+    for (int l0 = 0; l0 < c.n_layers; l0 += kMaxLayersPerKvLaunch) {  // K/V of every layer
+      const int nl = std::min(kMaxLayersPerKvLaunch, c.n_layers - l0);
+      GemvParams P{};
+      gemv_common(h, P);
+      P.n_amaps = 2 * nl;
+      for (int i = 0; i < nl; ++i) {
+        P.amap[2 * i] = h->m_wk[l0 + i];
+        P.amap[2 * i + 1] = h->m_wv[l0 + i];
+      }
+      for (int i = 0; i <= 2 * nl; ++i) P.tile_start[i] = i * tkv;
+      P.T = 2 * nl * tkv;
+      P.KB = H / 64;
+      P.bmap = h->m_cfeat[nb_index(nb)];
+      P.b_row0 = 0;
+      P.grow0 = row0;
+      P.op = OP_KV;
+      P.ss_in = h->at<float>(h->L.ss_fc);
+      P.ss_parts = H / 128;
+      P.ss_stride = kMaxPassRows;
+      P.ss_row0 = 0;
+      P.rope_cos = h->at<float>(h->L.rope_cos);
+      P.rope_sin = h->at<float>(h->L.rope_sin);
+      P.d = d;
+      P.kc = h->kc + static_cast<size_t>(l0) * c.max_batch * c.kv_capacity * c.n_kv_heads * d;
+      P.vc = h->vc + static_cast<size_t>(l0) * c.max_batch * c.kv_capacity * c.n_kv_heads * d;
+      P.nkv = c.n_kv_heads;
+      P.cap = c.kv_capacity;
+      P.max_batch = c.max_batch;
+      P.len = h->len;
+      P.n_new = n_new;
+      P.rows_per_seq = rows_per_seq;
+      P.batch = batch;
+      P.commit_len = (p == n_pass - 1) && (l0 + nl == c.n_layers);
+      DFL_TRY(run_gemv(h, P, nb, st));
+    }
+  }
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* drafted, float* logits,
+                       float* x_trace, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  if (batch < 1 || block < 1 || (block > 1 && !drafted)) return DFLASH_E_INVAL;
+  if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_launches = 0;
+  const int rows = batch * block;
+  const int H = c.hidden, d = c.head_dim, L = c.n_layers, R = h->L.R;
+  const int tq = c.n_heads * d / 128, tk = c.n_kv_heads * d / 128;
+  const size_t layer_elems = static_cast<size_t>(c.max_batch) * c.kv_capacity * c.n_kv_heads * d;
+  {
+    EmbedParams E{};
+    E.embed = static_cast<const __nv_bfloat16*>(h->w.embed);
+    E.mask_emb = static_cast<const __nv_bfloat16*>(h->w.mask_emb);
+    E.gain = static_cast<const __nv_bfloat16*>(h->layers[0].g_attn);
+    E.last_token = h->last_token;
+    E.len = h->len;
+    E.x = h->at<float>(h->L.x);
+    E.xg = h->at<__nv_bfloat16>(h->L.xg);
+    E.ss = h->at<float>(h->L.ss_emb);
+    E.trace = x_trace;
+    E.err = h->at<int>(h->L.err);
+    E.B = block;
+    E.H = H;
+    E.V = c.vocab;
+    E.cap = c.kv_capacity;
+    if (launch_embed(E, batch, st, true) != 0) return DFLASH_E_CUDA;
+    ++h->last_launches;
+  }
+  // rows are processed in passes of at most kMaxPassRows (one MMA N per pass)
+  auto for_passes = [&](auto&& fn) -> int {
+    for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {
+      const int pr = std::min(kMaxPassRows, rows - row0);
+      DFL_TRY(fn(row0, nb_for_rows(pr)));
+    }
+    return DFLASH_OK;
+  };
+  auto base = [&](GemvParams& P, int row0, int nb, const CUtensorMap& bmap) {
+    gemv_common(h, P);
+    P.bmap = bmap;
+    P.b_row0 = row0;
+    P.grow0 = row0;
+    P.out_row0 = row0;
+    P.ss_row0 = row0;
+    P.n_valid = rows;
+    P.rows_per_seq = block;
+    P.batch = batch;
+    (void)nb;
+  };
+  for (int l = 0; l < L; ++l) {
+    DFL_TRY(for_passes([&](int row0, int nb) {  // q, k, v with RoPE; block k/v into the cache
+      GemvParams P{};
+      base(P, row0, nb, h->m_xg[nb_index(nb)]);
+      P.amap[0] = h->m_wq[l];
+      P.amap[1] = h->m_wk[l];
+      P.amap[2] = h->m_wv[l];
+      P.n_amaps = 3;
+      P.tile_start[0] = 0;
+      P.tile_start[1] = tq;
+      P.tile_start[2] = tq + tk;
+      P.tile_start[3] = tq + 2 * tk;
+      P.T = tq + 2 * tk;
+      P.KB = H / 64;
+      P.op = OP_QKV;
+      if (l == 0) {
+        P.ss_in = h->at<float>(h->L.ss_emb);
+        P.ss_parts = 1;
+      } else {
+        P.ss_in = h->at<float>(h->L.ss_x);
+        P.ss_parts = H / 128;
+      }
+      P.ss_stride = R;
+      P.yb = h->at<__nv_bfloat16>(h->L.q);
+      P.yb_ld = c.n_heads * d;
+      P.rope_cos = h->at<float>(h->L.rope_cos);
+      P.rope_sin = h->at<float>(h->L.rope_sin);
+      P.d = d;
+      P.kc = h->kc;
+      P.vc = h->vc;
+      P.nkv = c.n_kv_heads;
+      P.cap = c.kv_capacity;
+      P.max_batch = c.max_batch;
+      P.layer = l;
+      P.len = h->len;
+      return run_gemv(h, P, nb, st);
+    }));
+    {  // bidirectional attention over injected context + block
+      AttnParams A{};
+      A.kmap = h->m_kcache[l];
+      A.vmap = h->m_vcache[l];
+      A.q = h->at<__nv_bfloat16>(h->L.q);
+      A.o = h->at<__nv_bfloat16>(h->L.o);
+      A.len = h->len;
+      A.err = h->at<int>(h->L.err);
+      A.B = block;
+      A.nq = c.n_heads;
+      A.nkv = c.n_kv_heads;
+      A.d = d;
+      A.cap = c.kv_capacity;
+      A.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+      int split = h->n_sms / (batch * c.n_kv_heads);
+      split = std::max(1, std::min(8, split));
+      if (launch_attention(A, batch, split, st, true) != 0) return DFLASH_E_CUDA;
+      ++h->last_launches;
+    }
+    DFL_TRY(for_passes([&](int row0, int nb) {  // x += o · Woᵀ
+      GemvParams P{};
+      base(P, row0, nb, h->m_o[nb_index(nb)]);
+      P.amap[0] = h->m_wo[l];
+      P.n_amaps = 1;
+      P.tile_start[1] = H / 128;
+      P.T = H / 128;
+      P.KB = c.n_heads * d / 64;
+      P.op = OP_RESID;
+      P.y = h->at<float>(h->L.x);
+      P.y_ld = H;
+      P.yb = h->at<__nv_bfloat16>(h->L.xg);
+      P.yb_ld = H;
+      P.gain = static_cast<const __nv_bfloat16*>(h->layers[l].g_mlp);
+      P.ss_out = h->at<float>(h->L.ss_x);
+      P.ss_stride = R;
+      return run_gemv(h, P, nb, st);
+    }));
+    DFL_TRY(for_passes([&](int row0, int nb) {  // act = silu(gate) * up
+      GemvParams P{};
+      base(P, row0, nb, h->m_xg[nb_index(nb)]);
+      P.amap[0] = h->m_wg[l];
+      P.amap[1] = h->m_wu[l];
+      P.n_amaps = 2;
+      P.pair_mode = 1;
+      P.T = c.intermediate / 64;
+      P.KB = H / 64;
+      P.op = OP_SWIGLU;
+      P.ss_in = h->at<float>(h->L.ss_x);
+      P.ss_parts = H / 128;
+      P.ss_stride = R;
+      P.yb = h->at<__nv_bfloat16>(h->L.act);
+      P.yb_ld = c.intermediate;
+      return run_gemv(h, P, nb, st);
+    }));
+    DFL_TRY(for_passes([&](int row0, int nb) {  // x += act · W_downᵀ
+      GemvParams P{};
+      base(P, row0, nb, h->m_act[nb_index(nb)]);
+      P.amap[0] = h->m_wd[l];
+      P.n_amaps = 1;
+      P.tile_start[1] = H / 128;
+      P.T = H / 128;
+      P.KB = c.intermediate / 64;
+      P.op = OP_RESID;
+      P.y = h->at<float>(h->L.x);
+      P.y_ld = H;
+      P.yb = h->at<__nv_bfloat16>(h->L.xg);
+      P.yb_ld = H;
+      P.gain = static_cast<const __nv_bfloat16*>(l + 1 < L ? h->layers[l + 1].g_attn : h->w.g_final);
+      P.ss_out = h->at<float>(h->L.ss_x);
+      P.ss_stride = R;
+      P.trace = x_trace ? x_trace + static_cast<size_t>(l + 1) * rows * H : nullptr;
+      return run_gemv(h, P, nb, st);
+    }));
+  }
+  (void)layer_elems;
+  if (block > 1) {
+    DFL_TRY(for_passes([&](int row0, int nb) {  // final norm, LM head, argmax
+      GemvParams P{};
+      base(P, row0, nb, h->m_xg[nb_index(nb)]);
+      P.amap[0] = h->m_lm;
+      P.n_amaps = 1;
+      P.T = ceil_div(c.vocab, 128);
+      P.tile_start[1] = P.T;
+      P.KB = H / 64;
+      P.op = OP_LMHEAD;
+      P.ss_in = h->at<float>(h->L.ss_x);
+      P.ss_parts = H / 128;
+      P.ss_stride = R;
+      P.logits = logits;
+      P.vocab = c.vocab;
+      P.n_out = c.vocab;
+      P.best_v = h->at<float>(h->L.best_v);
+      P.best_i = h->at<int>(h->L.best_i);
+      P.drafted = drafted;
+      return run_gemv(h, P, nb, st);
+    }));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int32_t* drafted, int32_t batch,
+                         int32_t block, int32_t* accept_len, int32_t* committed, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  if (!target_logits || !accept_len || !committed || batch < 1 || block < 1 || (block > 1 && !drafted))
+    return DFLASH_E_INVAL;
+  if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
+  h->last_launches = 0;
+  VerifyParams P{};
+  P.logits = target_logits;
+  P.drafted = drafted;
+  P.accept_len = accept_len;
+  P.committed = committed;
+  P.last_token = h->last_token;
+  P.part_v = h->at<float>(h->L.vpart_v);
+  P.part_i = h->at<int>(h->L.vpart_i);
+  P.seq_cnt = h->at<int>(h->L.seq_cnt);
+  P.err = h->at<int>(h->L.err);
+  P.B = block;
+  P.V = c.vocab;
+  int chunks = std::max(1, std::min(kMaxChunks, ceil_div(2LL * h->n_sms, static_cast<long long>(batch) * block)));
+  P.chunk_len = static_cast<int>(align_up(static_cast<size_t>(ceil_div(c.vocab, chunks)), 1024));
+  P.chunks = ceil_div(c.vocab, P.chunk_len);
+  if (launch_verify(P, batch, static_cast<cudaStream_t>(stream), true) != 0) return DFLASH_E_CUDA;
+  ++h->last_launches;
+  return DFLASH_OK;
+}
+
+int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K, const void* X, int32_t rows,
+                       float* Y, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  if (!W || !X || !Y || !aligned16(W) || !aligned16(X) || n_out < 1 || K < 64 || K % 64 || rows < 1)
+    return DFLASH_E_INVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_launches = 0;
+  CUtensorMap mw;
+  if (!enc2d(&mw, W, K, n_out, 64)) return DFLASH_E_CUDA;
+  for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {
+    const int pr = std::min(kMaxPassRows, rows - row0);
+    const int nb = nb_for_rows(pr);
+    CUtensorMap mx;
+    if (!enc2d(&mx, X, K, rows, 16 * nb)) return DFLASH_E_CUDA;
+    GemvParams P{};
+    gemv_common(h, P);
+    P.amap[0] = mw;
+    P.n_amaps = 1;
+    P.T = ceil_div(n_out, 128);
+    P.tile_start[1] = P.T;
+    P.KB = K / 64;
+    P.bmap = mx;
+    P.b_row0 = row0;
+    P.grow0 = row0;
+    P.out_row0 = row0;
+    P.n_valid = rows;
+    P.n_out = n_out;
+    P.op = OP_PLAIN;
+    P.y = Y;
+    P.y_ld = n_out;
+    DFL_TRY(run_gemv(h, P, nb, st));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear) {
+  if (!h || !flags) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DFLASH_E_CUDA;
+  if (cudaMemcpy(flags, h->ws + h->L.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_E_CUDA;
+  if (clear && cudaMemset(h->ws + h->L.err, 0, 4) != cudaSuccess) return DFLASH_E_CUDA;
+  return DFLASH_OK;
+}
+
+int32_t dflash_last_launch_count(const dflash_handle* h) { return h ? h->last_launches : 0; }
+
+const char* dflash_status_string(int s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_E_INVAL: return "invalid argument";
+    case DFLASH_E_CONFIG: return "unsupported drafter shape";
+    case DFLASH_E_CAPACITY: return "capacity exceeded";
+    case DFLASH_E_CUDA: return "CUDA error";
+    case DFLASH_E_STATE: return "state not bound";
+  }
+  return "unknown status";
+}
+
+int dflash_synth_plant(float* logits, const int32_t* drafted, const uint8_t* plant_masks, int32_t n_steps,
+                       const int32_t* step_counter, int32_t batch, int32_t block, int32_t vocab, float bump,
+                       int32_t* saved, void* stream) {
+  if (!logits || !plant_masks || !step_counter || !saved || n_steps < 1 || batch < 1 || block < 1 || vocab < 1 ||
+      (block > 1 && !drafted))
+    return DFLASH_E_INVAL;
+  if (static_cast<long long>(batch) * block * vocab >= (1LL << 31)) return DFLASH_E_CAPACITY;
+  return launch_plant(logits, drafted, plant_masks, n_steps, step_counter, batch, block, vocab, bump, saved,
+                      static_cast<cudaStream_t>(stream)) == 0
+             ? DFLASH_OK
+             : DFLASH_E_CUDA;
+}
+
+int dflash_synth_unplant(float* logits, int32_t* step_counter, int32_t n_steps, int32_t batch, int32_t block,
+                         const int32_t* saved, void* stream) {
+  if (!logits || !step_counter || !saved || n_steps < 1 || batch < 1 || block < 1) return DFLASH_E_INVAL;
+  return launch_unplant(logits, step_counter, n_steps, batch, block, saved, static_cast<cudaStream_t>(stream)) == 0
+             ? DFLASH_OK
+             : DFLASH_E_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,614 @@
+// Weight-streaming GEMM for the DFlash draft path on sm_103a (tcgen05 + TMA + TMEM).
+//
+// At batch 1 every projection of the drafter (context fusion, K/V injection, Q/K/V, O,
+// SwiGLU gate/up/down, LM head) multiplies a large bf16 weight by at most 16 activation
+// rows: the cost is reading the weight once from HBM. The weight tile (128 output rows x
+// 64 k, 16 KB) is the M=128 A operand of tcgen05.mma and the activation rows are the
+// N = 16*NB operand, so a single MMA instruction consumes 4 KB of weights. The
+// per-projection work that follows (RMSNorm scaling, RoPE, KV-cache append, residual add,
+// SiLU gating, LM-head argmax) runs in the epilogue on the fp32 accumulators read back
+// from TMEM, so no projection output makes a second trip through HBM.
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0     TMA producer: weight tiles and activation tiles into an S-stage smem ring
+//   warp 1     TMEM allocation; lane 0 issues the MMAs (two TMEM accumulators)
+//   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows
+//
+// Work split: units (tile, k-block) are divided evenly over the grid ("stream-K"); a tile
+// covered by several CTAs is reduced by the last one to finish it, summing the partials
+// in CTA order, so the result is deterministic and the same for any row count.
+// With programmatic dependent launch the producer streams the first S weight tiles
+// before waiting for the previous kernel, hiding the kernel boundary behind HBM reads.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+template <int NB>
+struct GemvCfg {
+  static constexpr int ROWS = 16 * NB;            // MMA N
+  static constexpr int A_BYTES = 128 * 64 * 2;     // 16 KB weight tile
+  static constexpr int B_BYTES = ROWS * 64 * 2;    // activation tile
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = NB == 1 ? 11 : NB == 2 ? 10 : NB == 4 ? 8 : NB == 8 ? 6 : 4;
+  static constexpr int TMEM_COLS = 2 * ROWS < 32 ? 32 : 2 * ROWS;
+  static constexpr int XLD = 132;                  // padded row of the exchange buffers
+  static constexpr int EPI_BYTES = 2 * 16 * XLD * 4 + 3 * ROWS * 4;
+  static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 32;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(128, ROWS);
+};
+
+DEV float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+DEV __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
+
+// CTA whose unit range contains unit u (units split as floor(c*U/G)).
+DEV int cta_of_unit(uint32_t u, uint32_t U, int G) {
+  return static_cast<int>(((static_cast<uint64_t>(u) + 1) * G + U - 1) / U) - 1;
+}
+DEV uint32_t unit_begin(int c, uint32_t U, int G) {
+  return static_cast<uint32_t>(static_cast<uint64_t>(c) * U / G);
+}
+// Partial slot of CTA c for tile t: 2c for its first tile, 2c+1 for its last.
+DEV int part_slot(int c, int t, uint32_t U, int G, int KB) {
+  return (static_cast<int>(unit_begin(c, U, G) / KB) == t) ? 2 * c : 2 * c + 1;
+}
+
+DEV int map_of_tile(const GemvParams& P, int t) {
+  int i = 0;
+  while (i + 1 < P.n_amaps && t >= P.tile_start[i + 1]) ++i;
+  return i;
+}
+
+DEV void load_a(const GemvParams& P, int t, int kb, uint8_t* dst, uint64_t* bar, uint64_t pol) {
+  if (P.pair_mode) {
+    tma_load_2d(dst, &P.amap[0], bar, kb * 64, t * 64, pol);
+    tma_load_2d(dst + 8192, &P.amap[1], bar, kb * 64, t * 64, pol);
+  } else {
+    const int mi = map_of_tile(P, t);
+    const int row = (t - P.tile_start[mi]) * 128;
+    tma_load_2d(dst, &P.amap[mi], bar, kb * 64, row, pol);
+    tma_load_2d(dst + 8192, &P.amap[mi], bar, kb * 64, row + 64, pol);
+  }
+}
+
+DEV void load_b(const GemvParams& P, int kb, uint8_t* dst, uint64_t* bar, uint64_t pol) {
+  if (P.b3d) {
+    const int tap = kb / P.b_kb_per_tap;
+    const int col = (kb - tap * P.b_kb_per_tap) * 64;
+    tma_load_3d(dst, &P.bmap, bar, col, P.b_row0, tap, pol);
+  } else {
+    tma_load_2d(dst, &P.bmap, bar, kb * 64, P.b_row0, pol);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue helpers
+// Sum over the 128 tile rows of w[j]^2 for each of the 16 chunk rows; lane (e & 7) == 0 of
+// group j = e >> 3 gets row j's total. Fixed summation order.
+DEV float rows_sumsq(const float (&w)[16], int m, int e, float* red, int XLD) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) red[j * XLD + m] = w[j] * w[j];
+  named_bar_sync(1, 128);
+  const int j = e >> 3, part = e & 7;
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) s += red[j * XLD + part * 16 + k];
+  s += __shfl_down_sync(0xffffffffu, s, 4, 8);
+  s += __shfl_down_sync(0xffffffffu, s, 2, 8);
+  s += __shfl_down_sync(0xffffffffu, s, 1, 8);
+  named_bar_sync(1, 128);
+  return s;
+}
+
+// Rotate-half RoPE across the tile: row m pairs with row m ^ (d/2) of the same head.
+DEV void rope16(float (&val)[16], const int (&pos)[16], int m, int d, const float* cosT, const float* sinT,
+                float* xch, int XLD) {
+  const int half = d >> 1;
+  const int jh = m & (d - 1);
+  const int fi = jh & (half - 1);
+  const bool lo = jh < half;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xch[j * XLD + m] = val[j];
+  named_bar_sync(1, 128);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float p = xch[j * XLD + (m ^ half)];
+    const float c = cosT[pos[j] * half + fi];
+    const float s = sinT[pos[j] * half + fi];
+    val[j] = lo ? (val[j] * c - p * s) : (val[j] * c + p * s);
+  }
+  named_bar_sync(1, 128);
+}
+
+template <int NB>
+DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], int m, int e, float* xch,
+                        int* xchi, const float* s_inv, float* s_bv, int* s_bi) {
+  constexpr int XLD = GemvCfg<NB>::XLD;
+  const int lr0 = chunk * 16;          // local row of v[0]
+  const int gr0 = P.grow0 + lr0;       // global row of v[0]
+  switch (P.op) {
+    case OP_PLAIN: {
+      const int n = t * 128 + m;
+      if (n < P.n_out) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (gr0 + j < P.n_valid) P.y[static_cast<size_t>(P.out_row0 + lr0 + j) * P.y_ld + n] = v[j];
+      }
+    } break;
+
+    case OP_FC: {
+      const int f = t * 128 + m;
+      const float g = bf2f(P.gain[f]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) P.yb[static_cast<size_t>(P.out_row0 + lr0 + j) * P.yb_ld + f] = f2bf(v[j] * g);
+      const float s = rows_sumsq(v, m, e, xch, XLD);
+      if ((e & 7) == 0) P.ss_out[t * P.ss_stride + P.out_row0 + lr0 + (e >> 3)] = s;
+    } break;
+
+    case OP_KV: {
+      const int mi = map_of_tile(P, t);
+      const int layer = mi >> 1;
+      const bool is_v = mi & 1;
+      const int feat = (t - P.tile_start[mi]) * 128 + m;  // head*d + j within Wk / Wv
+      float val[16];
+      int pos[16];
+      bool ok[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        val[j] = v[j] * s_inv[lr0 + j];
+        const int gr = gr0 + j;
+        const int s = gr / P.rows_per_seq, r = gr - s * P.rows_per_seq;
+        int p = 0;
+        bool valid = false;
+        if (s < P.batch) {
+          const int nn = __ldcg(P.n_new + s);
+          if (r < nn) {
+            p = __ldcg(P.len + s) + r;
+            valid = true;
+            if (p >= P.cap) {
+              valid = false;
+              if (feat == 0) raise_flag(P.err, kDevCapacity);
+            }
+          }
+        }
+        ok[j] = valid;
+        pos[j] = valid ? p : 0;
+      }
+      if (!is_v) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
+      __nv_bfloat16* cache = is_v ? P.vc : P.kc;
+      const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (!ok[j]) continue;
+        const int gr = gr0 + j;
+        const int s = gr / P.rows_per_seq;
+        const size_t off = ((static_cast<size_t>(layer) * P.max_batch + s) * P.cap + pos[j]) * row_elems + feat;
+        cache[off] = f2bf(val[j]);
+      }
+    } break;
+
+    case OP_QKV: {
+      const int mi = map_of_tile(P, t);  // 0 = q, 1 = k, 2 = v
+      const int feat = (t - P.tile_start[mi]) * 128 + m;
+      const int B = P.rows_per_seq;
+      float val[16];
+      int pos[16];
+      bool ok[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        val[j] = v[j] * s_inv[lr0 + j];
+        const int gr = gr0 + j;
+        const int s = gr / B, i = gr - s * B;
+        int p = 0;
+        bool valid = gr < P.n_valid;
+        if (valid) {
+          p = __ldcg(P.len + s) + i;
+          if (p >= P.cap) {
+            valid = false;
+            if (feat == 0 && mi == 1) raise_flag(P.err, kDevCapacity);
+          }
+        }
+        ok[j] = valid;
+        pos[j] = valid ? p : 0;
+      }
+      if (mi < 2) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
+      if (mi == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (gr0 + j < P.n_valid) P.yb[static_cast<size_t>(gr0 + j) * P.yb_ld + feat] = f2bf(val[j]);
+      } else {
+        __nv_bfloat16* cache = (mi == 1) ? P.kc : P.vc;
+        const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (!ok[j]) continue;
+          const int s = (gr0 + j) / B;
+          const size_t off = ((static_cast<size_t>(P.layer) * P.max_batch + s) * P.cap + pos[j]) * row_elems + feat;
+          cache[off] = f2bf(val[j]);
+        }
+      }
+    } break;
+
+    case OP_RESID: {
+      const int f = t * 128 + m;
+      const float g = bf2f(P.gain[f]);
+      float w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int gr = gr0 + j;
+        w[j] = 0.f;
+        if (gr < P.n_valid) {
+          const size_t off = static_cast<size_t>(gr) * P.y_ld + f;
+          const float xo = __ldcg(P.y + off) + v[j];
+          P.y[off] = xo;
+          P.yb[static_cast<size_t>(gr) * P.yb_ld + f] = f2bf(xo * g);
+          if (P.trace) P.trace[off] = xo;
+          w[j] = xo;
+        }
+      }
+      const float s = rows_sumsq(w, m, e, xch, XLD);
+      if ((e & 7) == 0 && gr0 + (e >> 3) < P.n_valid) P.ss_out[t * P.ss_stride + gr0 + (e >> 3)] = s;
+    } break;
+
+    case OP_SWIGLU: {
+      float val[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        val[j] = v[j] * s_inv[lr0 + j];
+        xch[j * XLD + m] = val[j];
+      }
+      named_bar_sync(1, 128);
+      if (m < 64) {
+        const int i = t * 64 + m;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float gt = val[j];
+          const float up = xch[j * XLD + m + 64];
+          const float a = gt / (1.f + __expf(-gt)) * up;
+          if (gr0 + j < P.n_valid) P.yb[static_cast<size_t>(gr0 + j) * P.yb_ld + i] = f2bf(a);
+        }
+      }
+      named_bar_sync(1, 128);
+    } break;
+
+    case OP_LMHEAD: {
+      const int vid = t * 128 + m;
+      const bool vok = vid < P.vocab;
+      const int B = P.rows_per_seq;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float z = v[j] * s_inv[lr0 + j];
+        const int gr = gr0 + j;
+        if (P.logits && vok && gr < P.n_valid) {
+          const int s = gr / B, i = gr - s * B;
+          if (i >= 1) P.logits[(static_cast<size_t>(s) * (B - 1) + i - 1) * P.vocab + vid] = z;
+        }
+        xch[j * XLD + m] = vok ? z : -INFINITY;
+      }
+      named_bar_sync(1, 128);
+      const int j = e >> 3, part = e & 7;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int mm = part * 16 + k;
+        const float z = xch[j * XLD + mm];
+        if (z > bv) { bv = z; bi = t * 128 + mm; }
+      }
+#pragma unroll
+      for (int off = 4; off >= 1; off >>= 1) {
+        const float ov = __shfl_down_sync(0xffffffffu, bv, off, 8);
+        const int oi = __shfl_down_sync(0xffffffffu, bi, off, 8);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (part == 0) {
+        const int lr = lr0 + j;
+        if (bv > s_bv[lr] || (bv == s_bv[lr] && bi < s_bi[lr])) { s_bv[lr] = bv; s_bi[lr] = bi; }
+      }
+      named_bar_sync(1, 128);
+      (void)xchi;
+    } break;
+  }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ GemvParams P) {
+  using C = GemvCfg<NB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + C::STAGES * C::A_BYTES;
+  float* xch = reinterpret_cast<float*>(sB + C::STAGES * C::B_BYTES);
+  int* xchi = reinterpret_cast<int*>(xch + 16 * C::XLD);
+  float* s_inv = reinterpret_cast<float*>(xchi + 16 * C::XLD);
+  float* s_bv = s_inv + C::ROWS;
+  int* s_bi = reinterpret_cast<int*>(s_bv + C::ROWS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_bi + C::ROWS);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);  // [0] last-arrival flag, [1..2] wait ok by tile parity
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const uint32_t U = static_cast<uint32_t>(P.T) * P.KB;
+  const uint32_t u0 = unit_begin(c, U, G), u1 = unit_begin(c + 1, U, G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < P.n_amaps; ++i) tma_prefetch_desc(&P.amap[i]);
+    tma_prefetch_desc(&P.bmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t n = u1 - u0;
+      const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
+      for (uint32_t i = 0; i < pre; ++i) {  // weights do not depend on the previous kernel
+        const uint32_t u = u0 + i;
+        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+        load_a(P, u / P.KB, u % P.KB, sA + i * C::A_BYTES, &full[i], pol_w);
+      }
+      pdl_wait();
+      for (uint32_t i = 0; i < pre; ++i) {
+        const uint32_t u = u0 + i;
+        load_b(P, u % P.KB, sB + i * C::B_BYTES, &full[i], pol_x);
+      }
+      uint32_t issued = pre;
+      for (uint32_t i = pre; i < n; ++i) {
+        const uint32_t s = i % C::STAGES, r = i / C::STAGES;
+        if (!mbar_wait(&empty[s], (r - 1) & 1)) {
+          raise_flag(P.err, kDevTimeout);
+          break;
+        }
+        const uint32_t u = u0 + i;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        load_a(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
+        load_b(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+        ++issued;
+      }
+      // drain: every copy this thread issued has landed before the CTA may exit
+      const uint32_t first = issued > static_cast<uint32_t>(C::STAGES) ? issued - C::STAGES : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1)) {
+          raise_flag(P.err, kDevTimeout);
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      uint32_t i = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int t = static_cast<int>(u0 / P.KB); ok && static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+        const uint32_t ub = max(u0, static_cast<uint32_t>(t) * P.KB);
+        const uint32_t ue = min(u1, static_cast<uint32_t>(t + 1) * P.KB);
+        const int acc = lt & 1;
+        if (lt >= 2 && !mbar_wait(&tempty[acc], ((lt >> 1) - 1) & 1)) {
+          raise_flag(P.err, kDevTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * C::ROWS;
+        for (uint32_t u = ub; u < ue; ++u, ++i) {
+          const uint32_t s = i % C::STAGES, r = i / C::STAGES;
+          if (!mbar_wait(&full[s], r & 1)) {
+            raise_flag(P.err, kDevTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32), C::IDESC,
+                        (u > ub || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int e = threadIdx.x - 64;
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    pdl_wait();
+    if (P.ss_in) {
+      for (int r = e; r < C::ROWS; r += 128) {
+        float s = 0.f;
+        for (int p = 0; p < P.ss_parts; ++p) s += __ldcg(P.ss_in + p * P.ss_stride + P.ss_row0 + r);
+        s_inv[r] = rsqrtf(s / static_cast<float>(P.H) + P.eps);
+      }
+    }
+    for (int r = e; r < C::ROWS; r += 128) {
+      s_bv[r] = -INFINITY;
+      s_bi[r] = 0x7fffffff;
+    }
+    named_bar_sync(1, 128);
+    int lt = 0;
+    for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+      const int acc = lt & 1;
+      if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!s_misc[1 + acc]) {
+        if (e == 0) raise_flag(P.err, kDevTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int ca = cta_of_unit(static_cast<uint32_t>(t) * P.KB, U, G);
+      const int cb = cta_of_unit(static_cast<uint32_t>(t + 1) * P.KB - 1, U, G);
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ROWS;
+      if (ca == cb) {
+        for (int ch = 0; ch < NB; ++ch) {
+          float v[16];
+          tmem_ld16(taddr + ch * 16, v);
+          if (ch == NB - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          epilogue_apply<NB>(P, t, ch, v, m, e, xch, xchi, s_inv, s_bv, s_bi);
+        }
+      } else {
+        const int slot = part_slot(c, t, U, G, P.KB);
+        float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
+        for (int ch = 0; ch < NB; ++ch) {
+          float v[16];
+          tmem_ld16(taddr + ch * 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(ch * 16 + j) * 128 + m] = v[j];
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (e == 0) {
+          const int old = atomicAdd(P.tile_cnt + t, 1);
+          const int last = (old == cb - ca);
+          if (last) P.tile_cnt[t] = 0;
+          s_misc[0] = last;
+        }
+        named_bar_sync(1, 128);
+        if (s_misc[0]) {
+          __threadfence();
+          for (int ch = 0; ch < NB; ++ch) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int cc = ca; cc <= cb; ++cc) {
+              const float* src = P.part + static_cast<size_t>(part_slot(cc, t, U, G, P.KB)) * C::ROWS * 128;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (ch * 16 + j) * 128 + m);
+            }
+            epilogue_apply<NB>(P, t, ch, v, m, e, xch, xchi, s_inv, s_bv, s_bi);
+          }
+        }
+      }
+    }
+
+    // ------------------------------------------------ CTA-level completion hooks
+    if (P.op == OP_LMHEAD || (P.op == OP_KV && P.commit_len)) {
+      named_bar_sync(1, 128);
+      if (P.op == OP_LMHEAD) {
+        for (int r = e; r < C::ROWS; r += 128) {
+          P.best_v[c * kMaxPassRows + r] = s_bv[r];
+          P.best_i[c * kMaxPassRows + r] = s_bi[r];
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (e == 0) {
+        const int old = atomicAdd(P.cta_cnt, 1);
+        const int last = (old == G - 1);
+        if (last) *P.cta_cnt = 0;
+        s_misc[0] = last;
+      }
+      named_bar_sync(1, 128);
+      if (s_misc[0]) {
+        __threadfence();
+        if (P.op == OP_LMHEAD) {
+          const int B = P.rows_per_seq;
+          for (int r = e; r < C::ROWS; r += 128) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int cc = 0; cc < G; ++cc) {
+              const float ov = __ldcg(P.best_v + cc * kMaxPassRows + r);
+              const int oi = __ldcg(P.best_i + cc * kMaxPassRows + r);
+              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            const int gr = P.grow0 + r;
+            if (gr < P.n_valid) {
+              const int s = gr / B, i = gr - s * B;
+              if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
+            }
+          }
+        } else {
+          for (int s = e; s < P.batch; s += 128) {
+            const int nl = __ldcg(P.len + s) + __ldcg(P.n_new + s);
+            P.len[s] = nl < P.cap ? nl : P.cap;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int NB>
+static int launch_nb(const GemvParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = GemvCfg<NB>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, gemv_kernel<NB>, p));
+}
+
+int gemv_smem_bytes(int nb) {
+  switch (nb) {
+    case 1: return GemvCfg<1>::SMEM;
+    case 2: return GemvCfg<2>::SMEM;
+    case 4: return GemvCfg<4>::SMEM;
+    case 8: return GemvCfg<8>::SMEM;
+    case 16: return GemvCfg<16>::SMEM;
+  }
+  return -1;
+}
+
+int gemv_set_attributes() {
+  cudaError_t e = cudaSuccess;
+#define DFL_ATTR(NB)                                                                              \
+  if (e == cudaSuccess)                                                                           \
+    e = cudaFuncSetAttribute(gemv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                             GemvCfg<NB>::SMEM);
+  DFL_ATTR(1) DFL_ATTR(2) DFL_ATTR(4) DFL_ATTR(8) DFL_ATTR(16)
+#undef DFL_ATTR
+  return static_cast<int>(e);
+}
+
+int launch_gemv(const GemvParams& p, int nb, int n_ctas, cudaStream_t stream, bool pdl) {
+  switch (nb) {
+    case 1: return launch_nb<1>(p, n_ctas, stream, pdl);
+    case 2: return launch_nb<2>(p, n_ctas, stream, pdl);
+    case 4: return launch_nb<4>(p, n_ctas, stream, pdl);
+    case 8: return launch_nb<8>(p, n_ctas, stream, pdl);
+    case 16: return launch_nb<16>(p, n_ctas, stream, pdl);
+  }
+  return static_cast<int>(cudaErrorInvalidValue);
+}
+
+}  // namespace dfl

@@ -1,0 +1,141 @@
+// Internal interfaces between the kernels and the C ABI glue (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfl {
+
+// ---------------------------------------------------------------- weight-streaming GEMM
+// Y = X · Wᵀ over a weight matrix streamed once from HBM: the weight tile (128 output rows
+// x 64 k) is the 128-row A operand of tcgen05.mma, the <= 256 activation rows are the N
+// operand. Work is split "stream-K" style: the (tile, k-block) units are divided evenly
+// over the CTAs; a tile split between CTAs is reduced in a fixed order by whichever CTA
+// finishes it last, so results never depend on timing.
+enum GemvOp : int {
+  OP_PLAIN = 0,   // Y fp32
+  OP_FC = 1,      // context fusion: cfeat = bf16(F * g_ctx), per-tile sum of squares of F
+  OP_KV = 2,      // injection: scale by 1/rms, RoPE on K, append K/V to the cache
+  OP_QKV = 3,     // block q/k/v: scale by 1/rms, RoPE on q and k, q -> q_buf, k/v -> cache
+  OP_RESID = 4,   // x += acc; xg = bf16(x * gain); per-tile sum of squares of x
+  OP_SWIGLU = 5,  // act = bf16(silu(gate/rms) * up/rms)
+  OP_LMHEAD = 6,  // z = acc/rms; optional logits; running argmax; last CTA writes drafts
+};
+
+constexpr int kMaxAMaps = 16;
+constexpr int kMaxCtas = 256;      // workspace partial slots are sized for this many CTAs
+constexpr int kMaxPassRows = 256;  // activation rows per GEMM pass (MMA N <= 256)
+
+struct GemvParams {
+  CUtensorMap amap[kMaxAMaps];  // weight maps, box 64 (k) x 64 (rows), 128-byte swizzle
+  CUtensorMap bmap;             // activation map, box 64 (k) x 16*NB rows [x 1 tap]
+  int n_amaps;
+  int tile_start[kMaxAMaps + 1];  // map i covers tiles [tile_start[i], tile_start[i+1])
+  int pair_mode;                  // rows 0-63 of tile t from map 0 row 64t, rows 64-127 from map 1 row 64t
+  int T;                          // output tiles of 128 rows
+  int KB;                         // k-blocks of 64 per tile
+  int b3d;                        // B operand: 3-D map over [taps][rows][Ht]
+  int b_kb_per_tap;               // Ht / 64 when b3d
+  int b_row0;                     // row coordinate of the pass in the B operand
+  int grow0;                      // global row id of local row 0 (positions, validity)
+  int out_row0;                   // row of local row 0 in the output buffers
+  int ss_row0;                    // row of local row 0 in ss_in
+  int n_valid;                    // rows with global id < n_valid are real (draft ops)
+  int op;
+  int n_out;                      // valid output features (ragged vocab)
+  // split-K reduction state (workspace)
+  float* part;
+  int* tile_cnt;
+  int* cta_cnt;
+  int* err;
+  // RMSNorm folded into the epilogue: inv_rms[row] = rsqrt(sum_p ss_in[p*ss_stride + row] / H + eps)
+  const float* ss_in;
+  int ss_parts;
+  int ss_stride;
+  float* ss_out;  // [T][ss_stride]
+  float eps;
+  int H;
+  const __nv_bfloat16* gain;
+  // outputs
+  float* y;                 // PLAIN: Y; RESID: residual x
+  int y_ld;
+  __nv_bfloat16* yb;        // FC: cfeat; RESID: xg; SWIGLU: act; QKV: q
+  int yb_ld;
+  float* trace;             // RESID: optional residual trace
+  // RoPE and caches
+  const float* rope_cos;    // [cap][d/2]
+  const float* rope_sin;
+  int d;
+  __nv_bfloat16* kc;        // [L][max_batch][cap][nkv][d]
+  __nv_bfloat16* vc;
+  int nkv, cap, max_batch, layer;
+  int* len;
+  const int* n_new;
+  int rows_per_seq;         // KV: row stride per sequence; draft ops: block size B
+  int batch;
+  int commit_len;
+  // LM head
+  float* logits;
+  int vocab;
+  float* best_v;            // [kMaxCtas][kMaxPassRows]
+  int* best_i;
+  int* drafted;
+};
+
+// NB = activation row groups of 16 (1, 2, 4, 8 or 16). Returns cudaError_t.
+int launch_gemv(const GemvParams& p, int nb, int n_ctas, cudaStream_t stream, bool pdl);
+int gemv_smem_bytes(int nb);
+int gemv_set_attributes();
+
+// ---------------------------------------------------------------- block attention
+struct AttnParams {
+  CUtensorMap kmap;  // 3-D over this layer's K cache: {d, nkv, max_batch*cap}, box {64, 1, 64}
+  CUtensorMap vmap;
+  const __nv_bfloat16* q;  // [rows][nq*d], row = s*B + i, post-RoPE
+  __nv_bfloat16* o;        // [rows][nq*d]
+  const int* len;
+  int* err;
+  int B, nq, nkv, d, cap;
+  float scale_log2;        // log2(e) / sqrt(d)
+};
+int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
+int attn_set_attributes();
+
+// ---------------------------------------------------------------- small kernels
+struct EmbedParams {
+  const __nv_bfloat16* embed;     // [V][H]
+  const __nv_bfloat16* mask_emb;  // [H]
+  const __nv_bfloat16* gain;      // g_attn of layer 0
+  const int* last_token;
+  const int* len;
+  float* x;                       // [rows][H]
+  __nv_bfloat16* xg;              // [rows][H]
+  float* ss;                      // [rows]
+  float* trace;                   // [rows][H] or null
+  int* err;
+  int B, H, V, cap;
+};
+int launch_embed(const EmbedParams& p, int batch, cudaStream_t stream, bool pdl);
+
+struct VerifyParams {
+  const float* logits;  // [batch][B][V]
+  const int* drafted;   // [batch][B-1]
+  int* accept_len;
+  int* committed;
+  int* last_token;
+  float* part_v;        // [batch][B][chunks]
+  int* part_i;
+  int* seq_cnt;         // [batch]
+  int* err;
+  int B, V, chunks, chunk_len;
+};
+int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pdl);
+
+int launch_plant(float* logits, const int* drafted, const uint8_t* masks, int n_steps, const int* step,
+                 int batch, int B, int V, float bump, int* saved, cudaStream_t stream);
+int launch_unplant(float* logits, int* step, int n_steps, int batch, int B, const int* saved,
+                   cudaStream_t stream);
+
+}  // namespace dfl

@@ -1,0 +1,193 @@
+// Block initialisation, greedy verification and the synthetic-target harness kernels.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+// ---------------------------------------------------------------- block initialisation
+// Slot 0 of each sequence holds the last accepted token's embedding, slots 1..B-1 the
+// mask embedding (jansverre.net, "Hva gjør DFlash annerledes ...": the drafter denoises a
+// masked token block). Writes the fp32 residual x, its bf16 copy scaled by layer 0's
+// attention-norm gain (the next projection's operand) and each row's sum of squares.
+__global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int row = blockIdx.x;
+  const int s = row / P.B, i = row - s * P.B;
+  const __nv_bfloat16* src = P.mask_emb;
+  if (i == 0) {
+    int tok = __ldcg(P.last_token + s);
+    if (tok < 0 || tok >= P.V) {
+      if (threadIdx.x == 0) raise_flag(P.err, kDevToken);
+      tok = 0;
+    }
+    src = P.embed + static_cast<size_t>(tok) * P.H;
+    if (threadIdx.x == 0 && __ldcg(P.len + s) + P.B > P.cap) raise_flag(P.err, kDevCapacity);
+  }
+  float ss = 0.f;
+  for (int f = threadIdx.x; f < P.H; f += blockDim.x) {
+    const float x = __bfloat162float(src[f]);
+    const size_t off = static_cast<size_t>(row) * P.H + f;
+    P.x[off] = x;
+    P.xg[off] = __float2bfloat16_rn(x * __bfloat162float(P.gain[f]));
+    if (P.trace) P.trace[off] = x;
+    ss += x * x;
+  }
+  __shared__ float red[8];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    P.ss[row] = t;
+  }
+}
+
+int launch_embed(const EmbedParams& p, int batch, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch * p.B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, embed_kernel, p));
+}
+
+// ---------------------------------------------------------------- greedy verification
+// Row argmax of the target logits (lowest index on ties), then the longest prefix of
+// drafts matching it plus the bonus token (bpdata.com DFlash article, introduction: the
+// target accepts the longest valid prefix). Grid (chunks, B, batch): each CTA reduces one
+// chunk of one row; the last CTA of a sequence (arrival counter, no waiting) merges the
+// chunks and decides the acceptance.
+DEV void better(float& bv, int& bi, float ov, int oi) {
+  if (ov > bv || (ov == bv && oi < bi)) {
+    bv = ov;
+    bi = oi;
+  }
+}
+
+__global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int chunk = blockIdx.x, i = blockIdx.y, s = blockIdx.z;
+  const int B = P.B, V = P.V;
+  const float* row = P.logits + (static_cast<size_t>(s) * B + i) * V;
+  const int c0 = chunk * P.chunk_len;
+  const int c1 = min(V, c0 + P.chunk_len);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if ((V & 3) == 0) {
+    for (int k = c0 + 4 * static_cast<int>(threadIdx.x); k < c1; k += 4 * blockDim.x) {
+      const float4 q = __ldcs(reinterpret_cast<const float4*>(row + k));
+      better(bv, bi, q.x, k);
+      better(bv, bi, q.y, k + 1);
+      better(bv, bi, q.z, k + 2);
+      better(bv, bi, q.w, k + 3);
+    }
+  } else {
+    for (int k = c0 + static_cast<int>(threadIdx.x); k < c1; k += blockDim.x) better(bv, bi, __ldcs(row + k), k);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ov = __shfl_down_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_down_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
+  }
+  __shared__ float wv[8];
+  __shared__ int wi[8];
+  __shared__ int s_last;
+  __shared__ int g[16];
+  if ((threadIdx.x & 31) == 0) {
+    wv[threadIdx.x >> 5] = bv;
+    wi[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) better(bv, bi, wv[w], wi[w]);
+    const int slot = (s * B + i) * P.chunks + chunk;
+    P.part_v[slot] = bv;
+    P.part_i[slot] = bi;
+    __threadfence();
+    const int old = atomicAdd(P.seq_cnt + s, 1);
+    s_last = (old == B * P.chunks - 1);
+    if (s_last) P.seq_cnt[s] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < B) {
+    float v = -INFINITY;
+    int idx = 0x7fffffff;
+    for (int c = 0; c < P.chunks; ++c) {
+      const int slot = (s * B + threadIdx.x) * P.chunks + c;
+      better(v, idx, __ldcg(P.part_v + slot), __ldcg(P.part_i + slot));
+    }
+    g[threadIdx.x] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int j = 0;
+    while (j < B - 1 && __ldcg(P.drafted + s * (B - 1) + j) == g[j]) ++j;
+    const int tau = j + 1;
+    P.accept_len[s] = tau;
+    P.last_token[s] = g[j];
+    for (int k = 0; k < B; ++k) P.committed[s * B + k] = k < tau ? g[k] : -1;
+  }
+}
+
+int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.chunks, p.B, batch);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, verify_kernel, p));
+}
+
+// ---------------------------------------------------------------- synthetic target (harness)
+__global__ void plant_kernel(float* logits, const int* drafted, const uint8_t* masks, int n_steps,
+                             const int* step, int batch, int B, int V, float bump, int* saved) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= batch * B) return;
+  const int s = k / B, i = k - s * B;
+  int st = *step;
+  st = ((st % n_steps) + n_steps) % n_steps;
+  saved[2 * k] = -1;
+  if (i >= B - 1 || !masks[(static_cast<size_t>(st) * batch + s) * B + i]) return;
+  const int tok = drafted[s * (B - 1) + i];
+  if (tok < 0 || tok >= V) return;
+  const size_t off = (static_cast<size_t>(s) * B + i) * V + tok;
+  saved[2 * k] = static_cast<int>(off);
+  saved[2 * k + 1] = __float_as_int(logits[off]);
+  logits[off] += bump;
+}
+
+__global__ void unplant_kernel(float* logits, int* step, int n_steps, int batch, int B, const int* saved) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k < batch * B && saved[2 * k] >= 0) logits[saved[2 * k]] = __int_as_float(saved[2 * k + 1]);
+  if (k == 0) *step = (*step + 1) % n_steps;
+}
+
+int launch_plant(float* logits, const int* drafted, const uint8_t* masks, int n_steps, const int* step, int batch,
+                 int B, int V, float bump, int* saved, cudaStream_t stream) {
+  const int n = batch * B;
+  plant_kernel<<<(n + 255) / 256, 256, 0, stream>>>(logits, drafted, masks, n_steps, step, batch, B, V, bump, saved);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_unplant(float* logits, int* step, int n_steps, int batch, int B, const int* saved, cudaStream_t stream) {
+  const int n = batch * B;
+  unplant_kernel<<<(n + 255) / 256, 256, 0, stream>>>(logits, step, n_steps, batch, B, saved);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace dfl

@@ -1,0 +1,211 @@
+/*
+ * dflash.h — C ABI of the GB300 (sm_103a) DFlash draft-and-verify step.
+ *
+ * DFlash drafts a whole block of future tokens with a small block-diffusion drafter in
+ * one forward pass; the target verifies the block in parallel and keeps the longest
+ * valid prefix. The drafter is conditioned on the target: hidden states from several
+ * target layers are fused into one compact target-context feature, which is injected
+ * into the Key and Value projections of every draft layer, where it stays in the draft
+ * KV cache across drafting iterations.
+ *   - jansverre.net, "DFlash: slik kan spekulativ dekoding gi opptil 6x raskere
+ *     AI-inferens", section "Hva gjør DFlash annerledes enn vanlig spekulativ dekoding?"
+ *   - theaistack.guide, "DFlash Crea Blocchi Interi di Token Contemporaneamente ...",
+ *     sections "Come funziona il drafting a blocchi" and "L'idea chiave: Il target sa
+ *     meglio"
+ *   - bpdata.com DFlash article (Hungarian), introduction and section "Hogyan működik a
+ *     DFlash spekulatív dekódolás?"
+ *
+ * One step is three calls on one stream: dflash_inject_ctx -> dflash_draft_block ->
+ * (target forward, outside this library) -> dflash_verify_greedy.
+ *
+ * Conventions for every call:
+ *   - All device memory (weights, KV caches, per-sequence state, workspace, inputs and
+ *     outputs) is allocated and owned by the caller. The library allocates no device
+ *     memory at any point; it keeps only a host-side handle.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *     default stream) and return a status code. Errors that the host can see (null
+ *     pointers, sizes out of range, unsupported shapes) return before any launch.
+ *   - Per-sequence lengths and token ids live on the device, so a step never needs a
+ *     host synchronisation and can be captured in a CUDA graph. Errors found by a kernel
+ *     (a capacity overflow, a token id out of range, a bounded wait that gave up) set a
+ *     flag in the workspace; kernels then skip the offending writes. Read and clear it
+ *     with dflash_read_device_error().
+ *   - bf16 means IEEE bfloat16 stored as 16-bit words; all matrices are row-major.
+ *   - Device pointers handed to the library must be 16-byte aligned; weight and
+ *     activation row strides are multiples of 16 bytes by construction of the shapes
+ *     dflash_create accepts.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ------------------------------------------------ */
+#define DFLASH_OK 0
+#define DFLASH_E_INVAL (-1)    /* bad argument: null pointer, size out of range, misalignment */
+#define DFLASH_E_CONFIG (-2)   /* drafter shape not supported by these kernels */
+#define DFLASH_E_CAPACITY (-3) /* batch/block/rows beyond what the config or workspace holds */
+#define DFLASH_E_CUDA (-4)     /* a CUDA runtime or driver call failed */
+#define DFLASH_E_STATE (-5)    /* dflash_bind_state has not been called */
+
+/* ---- device error flag bits (dflash_read_device_error) ---------------------------- */
+#define DFLASH_DEV_TIMEOUT 1   /* a bounded wait inside a kernel gave up; its results are void */
+#define DFLASH_DEV_CAPACITY 2  /* a write past a sequence's KV capacity was skipped */
+#define DFLASH_DEV_TOKEN 4     /* a token id outside [0, vocab) was seen; the row was skipped */
+
+/* ---- drafter shape ---------------------------------------------------------------- */
+typedef struct dflash_config {
+  int32_t hidden;        /* H: drafter hidden size, multiple of 128 */
+  int32_t n_heads;       /* nq: query heads */
+  int32_t n_kv_heads;    /* nkv: key/value heads; nq % nkv == 0, nq/nkv <= 8 */
+  int32_t head_dim;      /* d: 64 or 128; nq*d and nkv*d multiples of 128 */
+  int32_t n_layers;      /* L: draft layers, 1..16 */
+  int32_t intermediate;  /* I: SwiGLU inner size, multiple of 64 */
+  int32_t vocab;         /* V: vocabulary size, >= 2 */
+  int32_t n_taps;        /* k: tapped target layers, 1..16 */
+  int32_t target_hidden; /* Ht: target hidden size, multiple of 64 */
+  float rope_theta;      /* RoPE base */
+  float rms_eps;         /* RMSNorm epsilon */
+  int32_t max_block;     /* largest block B accepted by draft/verify, 1..16 */
+  int32_t max_batch;     /* largest number of sequences per call, 1..256 */
+  int32_t kv_capacity;   /* positions per sequence in the KV cache */
+} dflash_config;
+
+/* ---- weights (device pointers, bf16, caller-owned, registered once) --------------- */
+typedef struct dflash_layer_weights {
+  const void* wq;     /* [nq*d, H]  query projection */
+  const void* wk;     /* [nkv*d, H] key projection; also projects the injected context */
+  const void* wv;     /* [nkv*d, H] value projection; also projects the injected context */
+  const void* wo;     /* [H, nq*d]  attention output projection */
+  const void* w_gate; /* [I, H]     SwiGLU gate */
+  const void* w_up;   /* [I, H]     SwiGLU up */
+  const void* w_down; /* [H, I]     SwiGLU down */
+  const void* g_attn; /* [H]        RMSNorm gain before attention */
+  const void* g_mlp;  /* [H]        RMSNorm gain before the MLP */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void* w_fc;     /* [H, k*Ht] fusion of the k concatenated target hidden states */
+  const void* g_ctx;    /* [H]       RMSNorm gain of the fused context feature */
+  const void* embed;    /* [V, H]    token embedding (slot 0 of a block) */
+  const void* mask_emb; /* [H]       mask embedding (slots 1..B-1 of a block) */
+  const void* g_final;  /* [H]       final RMSNorm gain */
+  const void* lm_head;  /* [V, H]    LM head */
+  const dflash_layer_weights* layers; /* host array of n_layers entries */
+} dflash_weights;
+
+typedef struct dflash_handle dflash_handle;
+
+/* Validate a shape without touching the GPU. Returns DFLASH_OK or DFLASH_E_CONFIG. */
+int dflash_config_check(const dflash_config* cfg);
+
+/* Workspace bytes dflash_bind_state needs for this shape (0 if the shape is invalid).
+ * The workspace holds activations, split-K partials, reduction counters, the RoPE
+ * tables and the device error flag. */
+size_t dflash_workspace_size(const dflash_config* cfg);
+
+/* Register a drafter. Copies the config, records the weight pointers (which must stay
+ * valid until dflash_destroy) and encodes their TMA descriptors on the host. Uses the
+ * current CUDA device. *out receives the handle. */
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
+
+/* Release the host handle. Device memory stays the caller's. */
+int dflash_destroy(dflash_handle* h);
+
+/* Bind caller-owned state:
+ *   k_cache, v_cache  bf16 [L][max_batch][kv_capacity][nkv][d], zero-initialised by the
+ *                     caller. K is stored after RoPE. Positions [len, len+B) are used as
+ *                     scratch for the block's own keys/values during a draft.
+ *   len               int32 [max_batch] injected positions per sequence (device)
+ *   last_token        int32 [max_batch] slot-0 token of the next block (device)
+ *   workspace         dflash_workspace_size(cfg) bytes, 256-byte aligned
+ * Fills the RoPE tables and clears the workspace (synchronous; call once before use). */
+int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* len,
+                      int32_t* last_token, void* workspace, size_t workspace_bytes);
+
+/* KV injection (theaistack.guide, "L'idea chiave: Il target sa meglio"): for every new
+ * position, concatenate the k tapped target hidden states (tap order), fuse them with
+ * w_fc, RMSNorm with g_ctx into the context feature c, project c with every layer's
+ * Wk and Wv, apply RoPE to the keys at their absolute positions and append K/V to the
+ * cache at len[s] + r; then len[s] += n_new[s].
+ *   hidden        bf16 [k][batch * rows_per_seq][Ht]; sequence s's new rows are rows
+ *                 s*rows_per_seq + r for r < n_new[s]
+ *   rows_per_seq  row stride between sequences in `hidden` (host int, >= 1)
+ *   n_new         int32 [batch] on the device, 0 <= n_new[s] <= rows_per_seq
+ * Rows past n_new[s] are read but never written anywhere. A sequence that would pass
+ * kv_capacity sets DFLASH_DEV_CAPACITY and its overflowing rows are skipped. The
+ * result for a row depends only on that row, so two incremental injections give
+ * bit-identical caches to one injection of the same positions. */
+int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq,
+                      const int32_t* n_new, int32_t batch, void* stream);
+
+/* One block-diffusion draft pass (jansverre.net, "Hva gjør DFlash annerledes enn vanlig
+ * spekulativ dekoding?": the whole masked block is denoised in a single forward pass).
+ * Slot 0 of sequence s embeds last_token[s]; slots 1..B-1 hold the mask embedding;
+ * slot i sits at position len[s] + i. Each layer: RMSNorm, Q/K/V projection with RoPE,
+ * bidirectional attention over the injected context [0, len[s]) and the block's own B
+ * keys, output projection, RMSNorm, SwiGLU MLP (pre-norm, residual adds); then the final
+ * RMSNorm, the LM head on slots 1..B-1 and argmax (lowest index on ties).
+ *   drafted   int32 [batch][B-1] out: d_1..d_{B-1}
+ *   logits    fp32 [batch][B-1][V] out, or NULL (parity checks only; costs bandwidth)
+ *   x_trace   fp32 [L+1][batch*B][H] out, or NULL: block input then the residual after
+ *             every layer (parity checks only)
+ * Needs len[s] + B <= kv_capacity (else DFLASH_DEV_CAPACITY and the sequence's cache
+ * writes are skipped). len is not changed. */
+int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* drafted,
+                       float* logits, float* x_trace, void* stream);
+
+/* Greedy verification (bpdata.com DFlash article, introduction: the target accepts the
+ * longest valid prefix): g_i = argmax target_logits[s][i] (lowest index on ties);
+ * j = the number of leading i with drafted[s][i] == g_i (i < B-1); tau = j + 1.
+ *   target_logits  fp32 [batch][B][V], finite
+ *   drafted        int32 [batch][B-1]
+ *   accept_len     int32 [batch] out: tau in [1, B]
+ *   committed      int32 [batch][B] out: g_0..g_{tau-1}, then -1
+ * Also writes last_token[s] = g_{tau-1} (the next block's slot 0). Committed tokens are
+ * always the target's own greedy tokens, so the output equals target-only greedy
+ * decoding. The caller injects the tau accepted positions on the next step. */
+int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int32_t* drafted,
+                         int32_t batch, int32_t block, int32_t* accept_len, int32_t* committed,
+                         void* stream);
+
+/* Weight-streaming bf16 GEMM of the draft path, exposed for testing the engine alone:
+ * Y[r][m] = sum_k X[r][k] * W[m][k] in fp32 accumulation.
+ *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (rows <= 256),
+ *   Y  fp32 [rows][n_out] out. Uses the handle's bound workspace for split-K partials. */
+int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K, const void* X,
+                       int32_t rows, float* Y, void* stream);
+
+/* Copy the device error flag to *flags (synchronises the handle's device); clear it when
+ * `clear` is non-zero. */
+int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear);
+
+/* Number of kernel launches the last call on this handle made. */
+int32_t dflash_last_launch_count(const dflash_handle* h);
+
+/* Human-readable text of a status code. */
+const char* dflash_status_string(int status);
+
+/* ---- synthetic target (benchmark harness, not part of DFlash) ---------------------
+ * Stand-in for a target model inside a timed, graph-captured step: planting raises the
+ * logit of drafted token d_{i+1} in row i by `bump` where plant_masks[step][s][i] != 0
+ * (the target agrees with the draft there); unplanting restores the saved logits and
+ * advances the device step counter (modulo n_steps).
+ *   logits [batch][B][V] fp32, drafted [batch][B-1], plant_masks uint8 [n_steps][batch][B],
+ *   step_counter int32 [1], saved: 2*batch*B int32 words of scratch. */
+int dflash_synth_plant(float* logits, const int32_t* drafted, const uint8_t* plant_masks,
+                       int32_t n_steps, const int32_t* step_counter, int32_t batch, int32_t block,
+                       int32_t vocab, float bump, int32_t* saved, void* stream);
+int dflash_synth_unplant(float* logits, int32_t* step_counter, int32_t n_steps, int32_t batch,
+                         int32_t block, const int32_t* saved, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

@@ -1,0 +1,96 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every function
+include/dflash.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from block_diffusion_drafter_kv_gb300 import binding as B
+from block_diffusion_drafter_kv_gb300.build import LIB_PATH, build
+from synth import QWEN3_8B, TINY
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return B.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dflash_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("dflash_inject_ctx", "dflash_draft_block", "dflash_verify_greedy", "dflash_create",
+              "dflash_bind_state", "dflash_workspace_size", "dflash_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (dflash_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    # and the binding knows every one of them
+    assert set(declared_functions()) == set(B.SIGNATURES)
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(B.DflashConfig) == 14 * 4
+    assert ctypes.sizeof(B.DflashLayerWeights) == 9 * 8
+    assert ctypes.sizeof(B.DflashWeights) == 7 * 8
+
+
+def _cfg(shape=TINY, **kw):
+    c = B.make_config(shape, 4, 1, 128)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value", [("hidden", 200), ("head_dim", 96), ("n_kv_heads", 3),
+                                         ("intermediate", 100), ("max_block", 17), ("max_block", 0),
+                                         ("n_layers", 0), ("target_hidden", 100), ("vocab", 1),
+                                         ("kv_capacity", 2), ("max_batch", 0)])
+def test_config_check_rejects(L, field, value):
+    c = _cfg(**{field: value})
+    assert L.dflash_config_check(ctypes.byref(c)) == -2
+    assert L.dflash_workspace_size(ctypes.byref(c)) == 0
+
+
+def test_config_check_accepts_the_workload_shapes(L):
+    from synth import LLAMA31_8B
+    for s, blk, bat, cap in ((TINY, 4, 1, 128), (QWEN3_8B, 16, 1, 3700), (QWEN3_8B, 16, 32, 9000),
+                             (LLAMA31_8B, 16, 4, 33100)):
+        c = B.make_config(s, blk, bat, cap)
+        assert L.dflash_config_check(ctypes.byref(c)) == 0
+        n = L.dflash_workspace_size(ctypes.byref(c))
+        assert 0 < n < (2 << 30)
+
+
+def test_null_arguments_fail_before_any_launch(L):
+    c = _cfg()
+    h = ctypes.c_void_p()
+    assert L.dflash_create(None, None, ctypes.byref(h)) == -1
+    assert L.dflash_create(ctypes.byref(c), None, ctypes.byref(h)) == -1
+    w = B.DflashWeights()  # all null pointers
+    assert L.dflash_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)) == -1
+    assert L.dflash_inject_ctx(None, None, 1, None, 1, None) == -1
+    assert L.dflash_draft_block(None, 1, 4, None, None, None, None) == -1
+    assert L.dflash_verify_greedy(None, None, None, 1, 4, None, None, None) == -1
+    assert L.dflash_destroy(None) == -1
+    assert L.dflash_synth_plant(None, None, None, 1, None, 1, 4, 8, 1.0, None, None) == -1
+
+
+def test_status_strings(L):
+    assert L.dflash_status_string(0) == b"ok"
+    assert L.dflash_status_string(-3) == b"capacity exceeded"
+    assert L.dflash_status_string(123) == b"unknown status"
