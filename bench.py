@@ -1,0 +1,562 @@
+#!/usr/bin/env python
+"""Throughput of the DFlash draft-and-verify step on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input: KV injection
+of the previous step's accepted positions, one block-diffusion draft pass (B = 16), the
+synthetic target's agreement plant, greedy verification. Default workload: the
+Qwen3-8B-shaped 5-layer drafter, batch 1, 2048 injected context positions, B = 16,
+planted agreement p = 0.8 (configs of the draft-step benchmark: seeded synthetic
+weights N(0, 0.02) and hidden states N(0, 1); no trained weights or datasets).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+
+Prints one JSON line (rank 0). With --impl reference the CPU oracle is timed instead.
+Timing: W untimed steps, then exactly K steps as CUDA-graph replays between CUDA events
+on the launching stream, barrier + synchronize on both sides, max over ranks. The
+weights streamed every step (3.4 GB) are far larger than L2 (129 MB), so no flush is
+needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify steps/s and drafted tok/s (B=16) with HBM/tensor roofline fraction"
+UNIT = "steps/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default="qwen3-8b-b1-ctx2048-B16")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=30.0)
+    ap.add_argument("--trace-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic traffic
+
+def gemv_launches(s, batch, B, tau):
+    """(label, bytes, flops) of every weight-streaming launch of one step, in launch order.
+    Bytes: the weight read once, the activation rows read once, the outputs written once."""
+    H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
+    rows = batch * B
+    out = []
+    kin = s.n_taps * s.target_hidden
+    out.append(("fc", 2 * H * kin + 2 * tau * kin + 2 * tau * H, 2 * tau * H * kin))
+    kv = 2 * s.n_layers * s.n_kv_heads * d
+    out.append(("kv", 2 * kv * H + 2 * tau * H + 2 * tau * kv, 2 * tau * kv * H))
+    for _ in range(s.n_layers):
+        nqkv = (s.n_heads + 2 * s.n_kv_heads) * d
+        out.append(("qkv", 2 * nqkv * H + 2 * rows * (H + nqkv), 2 * rows * nqkv * H))
+        out.append(("attn", None, None))
+        out.append(("o", 2 * H * s.n_heads * d + 2 * rows * s.n_heads * d + 4 * 2 * rows * H, 2 * rows * H * s.n_heads * d))
+        out.append(("gateup", 2 * 2 * I * H + 2 * rows * (H + I), 2 * rows * 2 * I * H))
+        out.append(("down", 2 * H * I + 2 * rows * I + 4 * 2 * rows * H, 2 * rows * H * I))
+    out.append(("lm_head", 2 * V * H + 2 * rows * H + 4 * batch * (B - 1), 2 * batch * (B - 1) * V * H))
+    return out
+
+
+def attn_bytes_flops(s, batch, B, n_ctx):
+    """KV read once per layer per sequence (context plus block keys), q read, o written."""
+    kvb = 2 * 2 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
+    qo = 2 * 2 * batch * B * s.n_heads * s.head_dim
+    fl = 4 * batch * B * s.n_heads * s.head_dim * (n_ctx + B)
+    return kvb + qo, fl
+
+
+def step_bytes_flops(s, batch, B, n_ctx, tau):
+    byt = fl = 0
+    for lab, b, f in gemv_launches(s, batch, B, tau):
+        if lab == "attn":
+            b, f = attn_bytes_flops(s, batch, B, n_ctx)
+        byt += b
+        fl += f
+    byt += 2 * s.hidden * batch                           # embedding rows
+    byt += 4 * batch * B * s.vocab                        # target logits read by verify
+    return byt, fl
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, period_ms=20):
+        self.samples = []
+        self.proc = None
+        self.period_ms = period_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", str(self.period_ms)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1, gpu_index=None):
+        rows = [(t, r) for t, r in self.samples if len(r) >= 9 and (gpu_index is None or r[0] == str(gpu_index))]
+        inside = [r for t, r in rows if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside and rows:   # a very short region: take the samples nearest to it
+            rows.sort(key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))
+            inside = [r for _, r in rows[:3]]
+            note = "timed region shorter than the sampling period; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------------ CPU oracle runs
+
+def oracle_steps(shape, bits, w, seed, n_steps, budget_s, ctx_hidden_bits, step_hidden_bits, noise, masks):
+    """Run the oracle on one sequence of the workload: an untimed prefill of the context,
+    then up to n_steps timed steps (inject previous tau rows, draft, verify) within budget_s.
+    Returns (steps_done, seconds)."""
+    import numpy as np
+    from oracle.dflash_ref import Oracle
+    from synth import inputs as I
+    o = Oracle(shape, bits)
+    st = o.new_sequence(w.ctx + (n_steps + 2) * w.block + w.block, last_token=1)
+    o.inject(st, ctx_hidden_bits)
+    tau_prev = 0
+    done, t_used = 0, 0.0
+    while done < n_steps:
+        t0 = time.perf_counter()
+        if tau_prev:
+            o.inject(st, step_hidden_bits[:, :tau_prev])
+        r = o.draft(st, w.block)
+        T = I.plant_logits(noise[None], r.drafted[None], masks[done % len(masks)][None])[0]
+        v = o.verify(st, T, r.drafted)
+        tau_prev = v.accept_len
+        t_used += time.perf_counter() - t0
+        done += 1
+        if t_used > budget_s:
+            break
+    return done, t_used
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main arms
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(a):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+    from synth import WORKLOADS
+    from synth import inputs as I
+    w = WORKLOADS[a.workload]
+    s = w.shape
+    weights = I.make_weights(s, a.seed)
+    bits = weights.bits()
+    ctx_bits = I.bf16_bits(I.make_hidden(s, w.ctx, a.seed, "ctx"))
+    step_bits = I.bf16_bits(I.make_hidden(s, w.block, a.seed, "step"))
+    noise = I.make_logit_noise(1, w.block, s.vocab, a.seed).numpy()[0][None]
+    masks = [I.make_plant_mask(1, w.block, w.p_plant, a.seed, f"plant.{i}")[0] for i in range(8)]
+    budget = 150.0
+    if a.warmup > 0:
+        oracle_steps(s, bits, w, a.seed, 1, budget, ctx_bits, step_bits, noise[0], masks)
+    n, secs = oracle_steps(s, bits, w, a.seed, a.steps, budget, ctx_bits, step_bits, noise[0], masks)
+    v = n / secs
+    cores = cpu_cores()
+    sample = (f"{n} of the requested {a.steps} oracle steps of the {w.name} workload (inject + B={w.block} draft "
+              f"+ verify, fp64 NumPy, one sequence) after an untimed prefill of {w.ctx} positions; "
+              f"warm-up capped at 1 step, time budget {budget:.0f} s")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": n,
+        "warmup": min(a.warmup, 1), "ms_per_step": 1e3 * secs / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "batch": 1, "block": w.block, "ctx": w.ctx},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_cuda(a):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    from block_diffusion_drafter_kv_gb300.build import build
+    from synth import WORKLOADS, weight_bytes
+    from synth import inputs as I
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        build()
+    if ws > 1:
+        dist.barrier()
+    build()
+    w = WORKLOADS[a.workload]
+    s, B, batch = w.shape, w.block, w.batch
+    log = (lambda *m: print(*m, file=sys.stderr, flush=True)) if rank == 0 else (lambda *m: None)
+    t_setup = time.time()
+    weights_cpu = I.make_weights(s, a.seed)
+    weights = weights_cpu.to("cuda")
+    ctx_lens = I.ragged_ctx(w, a.seed + rank)
+    ctx_max = int(ctx_lens.max())
+    cap = ctx_max + (a.warmup + a.steps + a.trace_steps + 4) * B + B
+    dr = BND.Drafter(s, weights, max_block=B, max_batch=batch, kv_capacity=cap)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    log(f"[bench] weights ready in {time.time() - t_setup:.1f}s; prefill {ctx_max} positions x {batch}")
+    # prefill: inject the whole context of every sequence
+    hid_ctx = I.make_hidden(s, batch * ctx_max, a.seed + rank, "ctx")
+    n_ctx = torch.as_tensor(ctx_lens, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        dr.inject(hid_ctx.cuda(), ctx_max, n_ctx, batch)
+        dr.last_token[:batch].copy_(torch.as_tensor(I.initial_tokens(batch, s.vocab, a.seed + rank)))
+    stream.synchronize()
+    del hid_ctx
+    len0 = dr.len.clone()
+    last0 = dr.last_token.clone()
+    # per-step inputs, resident in HBM before timing
+    n_masks = a.warmup + a.steps + a.trace_steps + 2
+    p = I.per_seq_p(w, a.seed + rank)
+    masks_np = np.stack([I.make_plant_mask(batch, B, p, a.seed + rank, f"plant.{i}") for i in range(n_masks)])
+    hid_step_cpu = I.make_hidden(s, batch * B, a.seed + rank, "step")
+    noise_cpu = I.make_logit_noise(batch, B, s.vocab, a.seed + rank)
+    hid_step = hid_step_cpu.cuda()
+    noise = noise_cpu.cuda()
+    masks = torch.as_tensor(masks_np, device="cuda")
+    accept = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    drafted = torch.zeros(batch, max(B - 1, 1), dtype=torch.int32, device="cuda")
+    committed = torch.zeros(batch, B, dtype=torch.int32, device="cuda")
+    step_ctr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    saved = torch.zeros(2 * batch * B, dtype=torch.int32, device="cuda")
+    launches = {}
+
+    def inject_draft():
+        dr.inject(hid_step, B, accept, batch)
+        launches["inject"] = dr.last_launch_count()
+        dr.draft(batch, B, drafted)
+        launches["draft"] = dr.last_launch_count()
+
+    def plant_verify():
+        BND.synth_plant(noise, drafted, masks, n_masks, step_ctr, batch, B, 10.0, saved)
+        dr.verify(noise, drafted, batch, B, accept, committed)
+        launches["verify"] = dr.last_launch_count()
+        BND.synth_unplant(noise, step_ctr, n_masks, batch, B, saved)
+        launches["synthetic_target"] = 2
+
+    def reset():
+        dr.len.copy_(len0)
+        dr.last_token.copy_(last0)
+        accept.zero_()
+        step_ctr.zero_()
+
+    with torch.cuda.stream(stream):   # eager run once (also loads the modules) before capture
+        inject_draft()
+        plant_verify()
+    stream.synchronize()
+    assert dr.device_error() == 0, "device error flag after the eager step"
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        inject_draft()
+        plant_verify()
+    per_step_launches = sum(launches.values())
+    with torch.cuda.stream(stream):
+        reset()
+    stream.synchronize()
+
+    # ---------------------------------------------------------------- timed region
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            g_step.replay()
+        reset()
+    stream.synchronize()
+    len_start = int(dr.len[:batch].sum())
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    th0 = time.monotonic()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(a.steps):
+            g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    th1 = time.monotonic()
+    if ws > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    time.sleep(0.1)
+    clocks.stop()
+    err = dr.device_error()
+    len_end = int(dr.len[:batch].sum())
+    tau_sum = (len_end - len_start) + int(accept[:batch].sum())
+    mean_tau = tau_sum / (a.steps * batch)
+    if ws > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / a.steps
+    value = ws * batch * a.steps / (ms_total / 1e3)
+    n_avg = len_start / batch + (len_end - len_start) / (2.0 * batch)
+    tau_avg = mean_tau
+    byt, fl = step_bytes_flops(s, batch, B, n_avg, tau_avg)
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    tens = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    t_hbm = byt / (hbm * 1e9)
+    t_ten = fl / (tens * 1e12)
+    step_roof = {"bound": "hbm" if t_hbm >= t_ten else "tensor", "bytes": byt, "flops": fl,
+                 "achieved_gbs": byt / (ms_step * 1e-3) / 1e9,
+                 "frac": max(t_hbm, t_ten) / (ms_step * 1e-3), "peak_gbs": hbm,
+                 "peak_kind": f"{pk_kind} hbm_gbs"}
+    log(f"[bench] {ms_step * 1e3:.1f} us/step, mean tau {mean_tau:.2f}, step roofline {step_roof['frac']:.3f}")
+
+    # ---------------------------------------------------------------- traced pass (per-kernel)
+    kern = {}
+    roof = None
+    if a.trace_steps > 0:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(64)]
+        for ev in evs:              # torch creates the CUDA event on its first record
+            ev.record(stream)
+        stream.synchronize()
+        dr.trace_events(evs)
+        labels_inj = ["fc", "kv"]
+        labels_dr = ["embed"] + ["qkv", "attn", "o", "gateup", "down"] * s.n_layers + ["lm_head"]
+        with torch.cuda.stream(stream):
+            reset()
+        stream.synchronize()
+        acc_t = {}
+
+        def collect(labels, n):
+            torch.cuda.synchronize()
+            for i in range(min(n, len(labels))):
+                acc_t.setdefault(labels[i], []).append(evs[i].elapsed_time(evs[i + 1]))
+
+        for _ in range(a.trace_steps):
+            n_ctx_now = float(dr.len[:batch].float().mean())
+            tau_now = float(accept[:batch].float().mean())
+            with torch.cuda.stream(stream):
+                dr.inject(hid_step, B, accept, batch)
+            collect(labels_inj, dr.last_launch_count())
+            with torch.cuda.stream(stream):
+                dr.draft(batch, B, drafted)
+            collect(labels_dr, dr.last_launch_count())
+            with torch.cuda.stream(stream):
+                BND.synth_plant(noise, drafted, masks, n_masks, step_ctr, batch, B, 10.0, saved)
+                dr.verify(noise, drafted, batch, B, accept, committed)
+            collect(["verify"], dr.last_launch_count())
+            with torch.cuda.stream(stream):
+                BND.synth_unplant(noise, step_ctr, n_masks, batch, B, saved)
+        dr.trace_events([])
+        stream.synchronize()
+        gl = gemv_launches(s, batch, B, tau_avg)
+        gbytes = {}
+        for lab, b, f in gl:
+            if b is not None:
+                gbytes.setdefault(lab, []).append(b)
+        ab, af = attn_bytes_flops(s, batch, B, n_avg)
+        sum_b = sum_t = 0.0
+        for lab, ts in acc_t.items():
+            per_step_launches_lab = labels_inj.count(lab) + labels_dr.count(lab) + (lab == "verify")
+            us = 1e3 * sum(ts) / len(ts)
+            bb = None
+            if lab in gbytes:
+                bb = gbytes[lab][0]
+                sum_b += bb * len(ts)
+                sum_t += sum(ts) * 1e-3
+            elif lab == "attn":
+                bb = ab
+            elif lab == "verify":
+                bb = 4 * batch * B * s.vocab
+            kern[lab] = {"us": round(us, 2), "launches_per_step": per_step_launches_lab,
+                         "gbs": round(bb / (us * 1e-6) / 1e9, 1) if bb else None}
+        achieved = sum_b / sum_t / 1e9
+        roof = {"bound": "hbm", "kernel": "gemv_kernel (weight-streaming tcgen05 GEMM, all projections)",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": None, "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)",
+                "timing": "per-launch CUDA events on the launching stream, launches serialised"}
+        log("[bench] per-kernel: " + json.dumps(kern))
+        with torch.cuda.stream(stream):
+            reset()
+        stream.synchronize()
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if not a.no_e2e:
+        hid_host = hid_step_cpu.pin_memory()
+        noise_host = noise_cpu.clone().pin_memory()
+        logits_dev = torch.empty_like(noise)
+        drafted_host = torch.empty(drafted.shape, dtype=torch.int32).pin_memory()
+        acc_host = torch.empty(batch, dtype=torch.int32).pin_memory()
+        com_host = torch.empty(batch, B, dtype=torch.int32).pin_memory()
+        gA, gB = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gA, stream=stream):
+            dr.inject(hid_step, B, accept, batch)
+            dr.draft(batch, B, drafted)
+        with torch.cuda.graph(gB, stream=stream):
+            dr.verify(logits_dev, drafted, batch, B, accept, committed)
+        with torch.cuda.stream(stream):
+            reset()
+        stream.synchronize()
+        nh = noise_host.numpy()
+
+        def e2e_step(k):
+            with torch.cuda.stream(stream):
+                hid_step.copy_(hid_host, non_blocking=True)
+                gA.replay()
+                drafted_host.copy_(drafted, non_blocking=True)
+            stream.synchronize()
+            d = drafted_host.numpy()
+            m = masks_np[k % n_masks]
+            planted = []
+            for si in range(batch):
+                for i in range(B - 1):
+                    if m[si, i]:
+                        planted.append((si, i, int(d[si, i])))
+                        nh[si, i, int(d[si, i])] += np.float32(10.0)
+            with torch.cuda.stream(stream):
+                logits_dev.copy_(noise_host, non_blocking=True)
+                gB.replay()
+                acc_host.copy_(accept, non_blocking=True)
+                com_host.copy_(committed, non_blocking=True)
+            stream.synchronize()
+            for si, i, tk in planted:
+                nh[si, i, tk] -= np.float32(10.0)
+
+        for k in range(min(a.warmup, 3)):
+            e2e_step(k)
+        with torch.cuda.stream(stream):
+            reset()
+        stream.synchronize()
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for k in range(a.steps):
+            e2e_step(k)
+        t1 = time.perf_counter()
+        el = t1 - t0
+        if ws > 1:
+            t = torch.tensor([el], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            el = float(t.item())
+        e2e = {"value": ws * batch * a.steps / el, "unit": UNIT,
+               "h2d_bytes_per_step": hid_host.numel() * 2 + noise_host.numel() * 4,
+               "d2h_bytes_per_step": drafted_host.numel() * 4 + acc_host.numel() * 4 + com_host.numel() * 4,
+               "ms_per_step": 1e3 * el / a.steps,
+               "path": "C ABI calls with pinned host buffers; host plants the synthetic target's agreement"}
+
+    # ---------------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and ws == 1 and not a.no_cpu_baseline:
+        ctx_bits = I.bf16_bits(I.make_hidden(s, w.ctx, a.seed, "ctx"))
+        step_bits = I.bf16_bits(hid_step_cpu[:, :B])
+        masks_l = [masks_np[i][0] for i in range(len(masks_np))]
+        t0 = time.perf_counter()
+        n, secs = oracle_steps(s, weights_cpu.bits(), w, a.seed, 50, a.cpu_budget_s, ctx_bits, step_bits,
+                               noise_cpu.numpy()[0], masks_l)
+        log(f"[bench] oracle: {n} steps in {secs:.1f}s (+ prefill, total {time.perf_counter() - t0:.1f}s)")
+        cpu = {"value": n / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n} oracle steps of this workload (one sequence: inject + B={B} draft + verify, fp64 "
+                         f"NumPy) after an untimed prefill of {w.ctx} positions"}
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+    clk = clocks.summary(th0, th1, gpu_index if gpu_index.isdigit() else None)
+    if rank == 0:
+        wb = weight_bytes(s)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden states and logits)",
+            "config": {"workload": w.name, "batch_per_gpu": batch, "block": B, "ctx": int(ctx_lens.mean()),
+                       "drafter": f"H{s.hidden} L{s.n_layers} nq{s.n_heads} nkv{s.n_kv_heads} d{s.head_dim} "
+                                  f"I{s.intermediate} V{s.vocab} k{s.n_taps}",
+                       "p_plant": w.p_plant, "parallelism": f"replicas x{ws}",
+                       "l2": f"inputs larger than L2: {sum(v for k, v in wb.items() if k != 'embed_row') / 1e9:.2f} "
+                             "GB of weights streamed per step, no flush",
+                       "launch": "one CUDA graph per step, programmatic dependent launch between kernels"},
+            "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
+            "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,
+            "clocks": clk, "device_error": err,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_cuda(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -50,6 +50,7 @@ SIGNATURES = {
                                      c_void_p]),
     "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32]),
     "dflash_last_launch_count": (c_int32, [c_void_p]),
+    "dflash_trace_events": (c_int32, [c_void_p, POINTER(c_void_p), c_int32]),
     "dflash_status_string": (ctypes.c_char_p, [c_int32]),
     "dflash_synth_plant": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
                                      c_float, c_void_p, c_void_p]),
@@ -169,6 +170,12 @@ class Drafter:
 
     def last_launch_count(self) -> int:
         return self.L.dflash_last_launch_count(self.h)
+
+    def trace_events(self, events) -> None:
+        """Record torch.cuda.Event objects around each launch of later calls ([] turns it off)."""
+        arr = (c_void_p * max(1, len(events)))(*[e.cuda_event for e in events])
+        self._trace_keep = (arr, list(events))
+        check(self.L.dflash_trace_events(self.h, arr, len(events)), "dflash_trace_events")
 
     def close(self):
         if getattr(self, "h", None):

@@ -158,6 +158,7 @@ struct dflash_handle {
   CUtensorMap m_xg[5]{}, m_cfeat[5]{}, m_act[5]{}, m_o[5]{};
   std::vector<CUtensorMap> m_kcache, m_vcache;
   int last_launches = 0;
+  std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
 
   template <typename T>
   T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -176,11 +177,23 @@ void gemv_common(const dflash_handle* h, GemvParams& P) {
   P.n_out = 0x7fffffff;
 }
 
+// Start of a call: reset the launch count; with tracing on, record event 0.
+void call_begin(dflash_handle* h, cudaStream_t st) {
+  h->last_launches = 0;
+  if (!h->trace_ev.empty()) cudaEventRecord(h->trace_ev[0], st);
+}
+
+// After each launch: count it; with tracing on, record the event that closes it.
+void note_launch(dflash_handle* h, cudaStream_t st) {
+  ++h->last_launches;
+  if (h->last_launches < static_cast<int>(h->trace_ev.size())) cudaEventRecord(h->trace_ev[h->last_launches], st);
+}
+
 int run_gemv(dflash_handle* h, const GemvParams& P, int nb, cudaStream_t st) {
   const long long U = static_cast<long long>(P.T) * P.KB;
   const int G = static_cast<int>(std::min<long long>(std::min(h->n_sms, kMaxCtas), U));
-  const int e = launch_gemv(P, nb, G, st, true);
-  ++h->last_launches;
+  const int e = launch_gemv(P, nb, G, st, h->trace_ev.empty());
+  note_launch(h, st);
   return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
 }
 
@@ -327,7 +340,7 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
   const long long total_rows = static_cast<long long>(batch) * rows_per_seq;
   if (total_rows >= (1LL << 31)) return DFLASH_E_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  h->last_launches = 0;
+  call_begin(h, st);
   const int pass_rows = h->inject_pass_rows;
   const int nb = pass_rows / 16;
   const int n_pass = ceil_div(total_rows, pass_rows);
@@ -407,7 +420,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
   if (batch < 1 || block < 1 || (block > 1 && !drafted)) return DFLASH_E_INVAL;
   if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  h->last_launches = 0;
+  call_begin(h, st);
   const int rows = batch * block;
   const int H = c.hidden, d = c.head_dim, L = c.n_layers, R = h->L.R;
   const int tq = c.n_heads * d / 128, tk = c.n_kv_heads * d / 128;
@@ -428,8 +441,8 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     E.H = H;
     E.V = c.vocab;
     E.cap = c.kv_capacity;
-    if (launch_embed(E, batch, st, true) != 0) return DFLASH_E_CUDA;
-    ++h->last_launches;
+    if (launch_embed(E, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+    note_launch(h, st);
   }
   // rows are processed in passes of at most kMaxPassRows (one MMA N per pass)
   auto for_passes = [&](auto&& fn) -> int {
@@ -504,8 +517,8 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
       A.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
       int split = h->n_sms / (batch * c.n_kv_heads);
       split = std::max(1, std::min(8, split));
-      if (launch_attention(A, batch, split, st, true) != 0) return DFLASH_E_CUDA;
-      ++h->last_launches;
+      if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+      note_launch(h, st);
     }
     DFL_TRY(for_passes([&](int row0, int nb) {  // x += o · Woᵀ
       GemvParams P{};
@@ -596,7 +609,8 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   if (!target_logits || !accept_len || !committed || batch < 1 || block < 1 || (block > 1 && !drafted))
     return DFLASH_E_INVAL;
   if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
-  h->last_launches = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  call_begin(h, st);
   VerifyParams P{};
   P.logits = target_logits;
   P.drafted = drafted;
@@ -612,8 +626,8 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   int chunks = std::max(1, std::min(kMaxChunks, ceil_div(2LL * h->n_sms, static_cast<long long>(batch) * block)));
   P.chunk_len = static_cast<int>(align_up(static_cast<size_t>(ceil_div(c.vocab, chunks)), 1024));
   P.chunks = ceil_div(c.vocab, P.chunk_len);
-  if (launch_verify(P, batch, static_cast<cudaStream_t>(stream), true) != 0) return DFLASH_E_CUDA;
-  ++h->last_launches;
+  if (launch_verify(P, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+  note_launch(h, st);
   return DFLASH_OK;
 }
 
@@ -624,7 +638,7 @@ int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K
   if (!W || !X || !Y || !aligned16(W) || !aligned16(X) || n_out < 1 || K < 64 || K % 64 || rows < 1)
     return DFLASH_E_INVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  h->last_launches = 0;
+  call_begin(h, st);
   CUtensorMap mw;
   if (!enc2d(&mw, W, K, n_out, 64)) return DFLASH_E_CUDA;
   for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {
@@ -663,6 +677,16 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear) {
 }
 
 int32_t dflash_last_launch_count(const dflash_handle* h) { return h ? h->last_launches : 0; }
+
+int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events) {
+  if (!h || n_events < 0 || (n_events > 0 && !events)) return DFLASH_E_INVAL;
+  h->trace_ev.clear();
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return DFLASH_E_INVAL;
+    h->trace_ev.push_back(static_cast<cudaEvent_t>(events[i]));
+  }
+  return DFLASH_OK;
+}
 
 const char* dflash_status_string(int s) {
   switch (s) {

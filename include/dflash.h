@@ -188,6 +188,14 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear);
 /* Number of kernel launches the last call on this handle made. */
 int32_t dflash_last_launch_count(const dflash_handle* h);
 
+/* Per-launch tracing. `events` holds n_events caller-created cudaEvent_t handles (as void*;
+ * n_events = 0 turns tracing off). While on, every call records events[0] on its stream
+ * before its first launch and events[i] right after its i-th launch (while i < n_events),
+ * so consecutive events bracket one kernel each. Launches are then fully serialised (no
+ * programmatic overlap), which makes the traced durations conservative. The events must
+ * outlive their use; the library does not own them. */
+int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events);
+
 /* Human-readable text of a status code. */
 const char* dflash_status_string(int status);
 
