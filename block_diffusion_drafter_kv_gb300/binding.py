@@ -52,6 +52,8 @@ SIGNATURES = {
     "dflash_last_launch_count": (c_int32, [c_void_p]),
     "dflash_trace_events": (c_int32, [c_void_p, POINTER(c_void_p), c_int32]),
     "dflash_status_string": (ctypes.c_char_p, [c_int32]),
+    "dflash_verify_greedy_noalloc": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                               c_void_p, c_void_p]),
     "dflash_synth_plant": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32,
                                      c_float, c_void_p, c_void_p]),
     "dflash_synth_unplant": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
@@ -187,6 +189,14 @@ class Drafter:
             self.close()
         except Exception:
             pass
+
+
+def verify_greedy_noalloc(target_logits, drafted, batch: int, block: int, accept_len, committed, last_token,
+                          stream=None):
+    """Greedy verification with no handle and no allocation (scratch is a fixed array in the library)."""
+    check(lib().dflash_verify_greedy_noalloc(target_logits.data_ptr(), _ptr(drafted), batch, block,
+                                             target_logits.shape[-1], accept_len.data_ptr(), committed.data_ptr(),
+                                             last_token.data_ptr(), _stream(stream)), "dflash_verify_greedy_noalloc")
 
 
 def synth_plant(logits, drafted, masks, n_steps: int, step_counter, batch: int, block: int, bump: float, saved,

@@ -199,6 +199,33 @@ int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events)
 /* Human-readable text of a status code. */
 const char* dflash_status_string(int status);
 
+/* ---- greedy verification without any allocation -----------------------------------
+ * The DFlash pages have no counterpart for this entry point; it exists for callers that
+ * cannot allocate device memory at all, so cannot provide the workspace that
+ * dflash_verify_greedy reads through a bound handle. Typical cases: code running inside
+ * another inference engine whose memory pool forbids new allocations during decoding,
+ * or a process that is only handed the logits and token buffers.
+ *
+ * Same result as dflash_verify_greedy (g_i = row argmax with the lowest index on ties;
+ * tau = 1 + number of leading drafts equal to g_i; committed = g_0..g_{tau-1}, then -1)
+ * and last_token[s] = g_{tau-1} is written to the caller's array. No handle is needed.
+ * Its scratch (argmax partials and arrival counters, about 257 KB) is one fixed array
+ * inside the library, which every GPU that loads the library keeps until the process
+ * exits. Limits: batch <= DFLASH_NOALLOC_MAX_BATCH, block <= 16; larger sizes return
+ * DFLASH_E_CAPACITY before anything is launched. It allocates no memory and calls no
+ * allocating routine.
+ *   - The first call on each device looks up the array's device address (a host-side
+ *     symbol lookup); make that first call before any stream capture.
+ *   - All calls share the one array. Calls whose work overlaps on the GPU (different
+ *     streams without ordering, or different host threads) race and give wrong results;
+ *     order them on one stream. Each call clears the counters it needs, so the
+ *     contents left by an earlier call do not matter. */
+#define DFLASH_NOALLOC_MAX_BATCH 64
+#define DFLASH_NOALLOC_MAX_CHUNKS 32
+int dflash_verify_greedy_noalloc(const float* target_logits, const int32_t* drafted, int32_t batch,
+                                 int32_t block, int32_t vocab, int32_t* accept_len, int32_t* committed,
+                                 int32_t* last_token, void* stream);
+
 /* ---- synthetic target (benchmark harness, not part of DFlash) ---------------------
  * Stand-in for a target model inside a timed, graph-captured step: planting raises the
  * logit of drafted token d_{i+1} in row i by `bump` where plant_masks[step][s][i] != 0
