@@ -89,32 +89,43 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     tma_prefetch_desc(&P.vmap);
   }
   __syncthreads();
-  pdl_wait();
-  pdl_launch_dependents();
 
-  int nkeys = __ldcg(P.len + seq) + B;
+  // The kernel before this one (the Q/K/V projection) starts only after the injection of
+  // this step has completed, so len and the injected context keys [0, len) are final here;
+  // only q and the block's own keys [len, len+B) are still being written. Tiles entirely
+  // below len are therefore fetched before waiting on the previous kernel.
+  const int len = __ldcg(P.len + seq);
+  int nkeys = len + B;
   if (nkeys > P.cap) nkeys = P.cap;
   const int ntiles = (nkeys + KT - 1) / KT;
   const int t0 = rank * ntiles / S, t1 = (rank + 1) * ntiles / S;
   const int n = t1 - t0;
   const int key_row0 = seq * P.cap;
+  const int pre = n < STAGES ? n : STAGES;
 
-  // prologue: the first STAGES key tiles (the KV cache is kept in L2 with evict_last)
-  if (threadIdx.x == 0) {
-    const int pre = n < STAGES ? n : STAGES;
-    for (int i = 0; i < pre; ++i) {
-      const int st = i % STAGES;
-      uint8_t* kd = smem + st * 2 * TILE_BYTES;
-      uint8_t* vd = kd + TILE_BYTES;
-      const int row = key_row0 + (t0 + i) * KT;
-      const uint64_t pol = policy_evict_last();
-      mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
+  auto issue = [&](int i, uint64_t pol) {
+    const int st = i % STAGES;
+    uint8_t* kd = smem + st * 2 * TILE_BYTES;
+    uint8_t* vd = kd + TILE_BYTES;
+    const int row = key_row0 + (t0 + i) * KT;
+    mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
 #pragma unroll
-      for (int b = 0; b < NBOX; ++b) {
-        tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
-        tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
-      }
+    for (int b = 0; b < NBOX; ++b) {
+      tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
+      tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
     }
+  };
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_last();
+    for (int i = 0; i < pre; ++i)
+      if ((t0 + i + 1) * KT <= len) issue(i, pol);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_last();
+    for (int i = 0; i < pre; ++i)
+      if ((t0 + i + 1) * KT > len) issue(i, pol);
   }
 
   // Q fragments of this warp's head: rows = block slots (>= B are zero).
@@ -237,18 +248,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
         *s_abort = 1;
         raise_flag(P.err, kDevTimeout);
       }
-      if (!*s_abort) {
-        const uint64_t pol = policy_evict_last();
-        uint8_t* kd = smem + st * 2 * TILE_BYTES;
-        uint8_t* vd = kd + TILE_BYTES;
-        const int row = key_row0 + (t0 + i + STAGES) * KT;
-        mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
-#pragma unroll
-        for (int b = 0; b < NBOX; ++b) {
-          tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
-          tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
-        }
-      }
+      if (!*s_abort) issue(i + STAGES, policy_evict_last());
     }
   }
 

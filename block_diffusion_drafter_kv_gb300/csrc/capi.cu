@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -144,6 +145,7 @@ struct dflash_handle {
   int device = 0;
   int n_sms = 0;
   int inject_pass_rows = 16;
+  int gemv_pref = 2;  // weight-streaming kernel variant for single-row-group launches
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -189,10 +191,19 @@ void note_launch(dflash_handle* h, cudaStream_t st) {
   if (h->last_launches < static_cast<int>(h->trace_ev.size())) cudaEventRecord(h->trace_ev[h->last_launches], st);
 }
 
-int run_gemv(dflash_handle* h, const GemvParams& P, int nb, cudaStream_t st) {
+// P.KB arrives in 64-wide k-blocks; the chosen kernel variant may stage several per step.
+int run_gemv(dflash_handle* h, const GemvParams& P0, int nb, cudaStream_t st) {
+  GemvParams P = P0;
+  int v = gemv_variant(nb, h->gemv_pref);
+  int ks = gemv_variant_ksub(v);
+  if (P.KB % ks != 0) {
+    v = gemv_variant(nb, 0);
+    ks = gemv_variant_ksub(v);
+  }
+  P.KB /= ks;
   const long long U = static_cast<long long>(P.T) * P.KB;
   const int G = static_cast<int>(std::min<long long>(std::min(h->n_sms, kMaxCtas), U));
-  const int e = launch_gemv(P, nb, G, st, h->trace_ev.empty());
+  const int e = launch_gemv(P, v, G, st, h->trace_ev.empty());
   note_launch(h, st);
   return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
 }
@@ -210,7 +221,7 @@ extern "C" {
 int dflash_config_check(const dflash_config* c) {
   if (!c) return DFLASH_E_INVAL;
   const int d = c->head_dim;
-  bool ok = c->hidden >= 128 && c->hidden % 128 == 0 && c->n_heads >= 1 && c->n_kv_heads >= 1 &&
+  bool ok = c->hidden >= 128 && c->hidden % 128 == 0 && c->hidden <= 8192 && c->n_heads >= 1 && c->n_kv_heads >= 1 &&
             c->n_heads % c->n_kv_heads == 0 && c->n_heads / c->n_kv_heads <= 8 && (d == 64 || d == 128) &&
             (c->n_heads * d) % 128 == 0 && (c->n_kv_heads * d) % 128 == 0 && c->n_layers >= 1 &&
             c->n_layers <= 16 && c->intermediate >= 64 && c->intermediate % 64 == 0 && c->vocab >= 2 &&
@@ -246,6 +257,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->w = *w;
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
+  if (const char* ev = std::getenv("DFLASH_GEMV_VARIANT")) h->gemv_pref = std::atoi(ev);
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
       gemv_set_attributes() != 0 || attn_set_attributes() != 0) {

@@ -24,16 +24,24 @@
 
 namespace dfl {
 
-template <int NB>
+// NB: activation row groups of 16 (MMA N = 16*NB). KSUB: 64-wide k-boxes per pipeline
+// stage (a stage holds 128 weight rows x 64*KSUB k, so each weight row contributes
+// 128*KSUB contiguous bytes per stage). STAGES: depth of the shared-memory ring.
+// MINB: CTAs per SM the launch bounds are sized for.
+template <int NB, int KSUB, int STAGES_, int MINB_>
 struct GemvCfg {
-  static constexpr int ROWS = 16 * NB;            // MMA N
-  static constexpr int A_BYTES = 128 * 64 * 2;     // 16 KB weight tile
-  static constexpr int B_BYTES = ROWS * 64 * 2;    // activation tile
+  static constexpr int ROWS = 16 * NB;               // MMA N
+  static constexpr int KS = KSUB;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int MINB = MINB_;
+  static constexpr int A_SUB = 128 * 64 * 2;          // one 128 x 64 weight sub-tile (16 KB)
+  static constexpr int B_SUB = ROWS * 64 * 2;         // one ROWS x 64 activation sub-tile
+  static constexpr int A_BYTES = KSUB * A_SUB;
+  static constexpr int B_BYTES = KSUB * B_SUB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = NB == 1 ? 11 : NB == 2 ? 10 : NB == 4 ? 8 : NB == 8 ? 6 : 4;
   static constexpr int TMEM_COLS = 2 * ROWS < 32 ? 32 : 2 * ROWS;
-  static constexpr int XLD = 132;                  // padded row of the exchange buffers
-  static constexpr int EPI_BYTES = 2 * 16 * XLD * 4 + 3 * ROWS * 4;
+  static constexpr int XLD = 132;                     // padded row of the exchange buffer
+  static constexpr int EPI_BYTES = 16 * XLD * 4 + 3 * ROWS * 4;
   static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(128, ROWS);
@@ -60,25 +68,38 @@ DEV int map_of_tile(const GemvParams& P, int t) {
   return i;
 }
 
-DEV void load_a(const GemvParams& P, int t, int kb, uint8_t* dst, uint64_t* bar, uint64_t pol) {
+// Weight sub-tiles of k-stage ks (KSUB boxes of 64 k each, two 64-row boxes per sub-tile).
+template <int KSUB>
+DEV void load_a(const GemvParams& P, int t, int ks, uint8_t* dst, uint64_t* bar, uint64_t pol) {
+  int m0, m1, r0, r1;
   if (P.pair_mode) {
-    tma_load_2d(dst, &P.amap[0], bar, kb * 64, t * 64, pol);
-    tma_load_2d(dst + 8192, &P.amap[1], bar, kb * 64, t * 64, pol);
+    m0 = 0; m1 = 1; r0 = t * 64; r1 = t * 64;
   } else {
     const int mi = map_of_tile(P, t);
-    const int row = (t - P.tile_start[mi]) * 128;
-    tma_load_2d(dst, &P.amap[mi], bar, kb * 64, row, pol);
-    tma_load_2d(dst + 8192, &P.amap[mi], bar, kb * 64, row + 64, pol);
+    m0 = m1 = mi;
+    r0 = (t - P.tile_start[mi]) * 128;
+    r1 = r0 + 64;
+  }
+#pragma unroll
+  for (int j = 0; j < KSUB; ++j) {
+    const int k = (ks * KSUB + j) * 64;
+    tma_load_2d(dst + j * 16384, &P.amap[m0], bar, k, r0, pol);
+    tma_load_2d(dst + j * 16384 + 8192, &P.amap[m1], bar, k, r1, pol);
   }
 }
 
-DEV void load_b(const GemvParams& P, int kb, uint8_t* dst, uint64_t* bar, uint64_t pol) {
-  if (P.b3d) {
-    const int tap = kb / P.b_kb_per_tap;
-    const int col = (kb - tap * P.b_kb_per_tap) * 64;
-    tma_load_3d(dst, &P.bmap, bar, col, P.b_row0, tap, pol);
-  } else {
-    tma_load_2d(dst, &P.bmap, bar, kb * 64, P.b_row0, pol);
+template <int KSUB, int B_SUB>
+DEV void load_b(const GemvParams& P, int ks, uint8_t* dst, uint64_t* bar, uint64_t pol) {
+#pragma unroll
+  for (int j = 0; j < KSUB; ++j) {
+    const int kb = ks * KSUB + j;
+    if (P.b3d) {
+      const int tap = kb / P.b_kb_per_tap;
+      const int col = (kb - tap * P.b_kb_per_tap) * 64;
+      tma_load_3d(dst + j * B_SUB, &P.bmap, bar, col, P.b_row0, tap, pol);
+    } else {
+      tma_load_2d(dst + j * B_SUB, &P.bmap, bar, kb * 64, P.b_row0, pol);
+    }
   }
 }
 
@@ -120,10 +141,9 @@ DEV void rope16(float (&val)[16], const int (&pos)[16], int m, int d, const floa
   named_bar_sync(1, 128);
 }
 
-template <int NB>
+template <int NB, int XLD>
 DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], int m, int e, float* xch,
-                        int* xchi, const float* s_inv, float* s_bv, int* s_bi) {
-  constexpr int XLD = GemvCfg<NB>::XLD;
+                        const float* s_inv, float* s_bv, int* s_bi, const float (&xpre)[16]) {
   const int lr0 = chunk * 16;          // local row of v[0]
   const int gr0 = P.grow0 + lr0;       // global row of v[0]
   switch (P.op) {
@@ -239,7 +259,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         w[j] = 0.f;
         if (gr < P.n_valid) {
           const size_t off = static_cast<size_t>(gr) * P.y_ld + f;
-          const float xo = __ldcg(P.y + off) + v[j];
+          const float xo = (NB == 1 ? xpre[j] : __ldcg(P.y + off)) + v[j];
           P.y[off] = xo;
           P.yb[static_cast<size_t>(gr) * P.yb_ld + f] = f2bf(xo * g);
           if (P.trace) P.trace[off] = xo;
@@ -306,21 +326,19 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         if (bv > s_bv[lr] || (bv == s_bv[lr] && bi < s_bi[lr])) { s_bv[lr] = bv; s_bi[lr] = bi; }
       }
       named_bar_sync(1, 128);
-      (void)xchi;
     } break;
   }
 }
 
-template <int NB>
-__global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ GemvParams P) {
-  using C = GemvCfg<NB>;
+template <class C>
+__global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constant__ GemvParams P) {
+  constexpr int NB = C::ROWS / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + C::STAGES * C::A_BYTES;
   float* xch = reinterpret_cast<float*>(sB + C::STAGES * C::B_BYTES);
-  int* xchi = reinterpret_cast<int*>(xch + 16 * C::XLD);
-  float* s_inv = reinterpret_cast<float*>(xchi + 16 * C::XLD);
+  float* s_inv = xch + 16 * C::XLD;
   float* s_bv = s_inv + C::ROWS;
   int* s_bi = reinterpret_cast<int*>(s_bv + C::ROWS);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_bi + C::ROWS);
@@ -358,7 +376,12 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  pdl_launch_dependents();
+  // Every thread but the producer waits for the previous kernel now and then lets the next
+  // one start; the producer first streams weights that do not depend on it.
+  if (!(warp == 0 && lane == 0)) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -370,12 +393,15 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
       for (uint32_t i = 0; i < pre; ++i) {  // weights do not depend on the previous kernel
         const uint32_t u = u0 + i;
         mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-        load_a(P, u / P.KB, u % P.KB, sA + i * C::A_BYTES, &full[i], pol_w);
+        load_a<C::KS>(P, u / P.KB, u % P.KB, sA + i * C::A_BYTES, &full[i], pol_w);
       }
       pdl_wait();
+      // The grid this kernel depends on has completed, so everything it (or anything before
+      // it) wrote is visible: from here on the next kernel may start and prefetch.
+      pdl_launch_dependents();
       for (uint32_t i = 0; i < pre; ++i) {
         const uint32_t u = u0 + i;
-        load_b(P, u % P.KB, sB + i * C::B_BYTES, &full[i], pol_x);
+        load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + i * C::B_BYTES, &full[i], pol_x);
       }
       uint32_t issued = pre;
       for (uint32_t i = pre; i < n; ++i) {
@@ -386,8 +412,8 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
         }
         const uint32_t u = u0 + i;
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        load_a(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
-        load_b(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+        load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
+        load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
         ++issued;
       }
       // drain: every copy this thread issued has landed before the CTA may exit
@@ -425,9 +451,12 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
           const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32), C::IDESC,
-                        (u > ub || kk > 0) ? 1u : 0u);
+          for (int j = 0; j < C::KS; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32),
+                          smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), C::IDESC,
+                          (u > ub || j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
         }
         if (ok) tc_commit(&tfull[acc]);
@@ -440,10 +469,18 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
     const int m = q * 32 + lane;
     pdl_wait();
     if (P.ss_in) {
-      for (int r = e; r < C::ROWS; r += 128) {
-        float s = 0.f;
-        for (int p = 0; p < P.ss_parts; ++p) s += __ldcg(P.ss_in + p * P.ss_stride + P.ss_row0 + r);
-        s_inv[r] = rsqrtf(s / static_cast<float>(P.H) + P.eps);
+      // inv_rms of every row of the pass: 8 lanes per row each sum a strided subset of the
+      // per-tile partials (all loads in flight at once), then a fixed lane tree combines them.
+      for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
+        const int r = r0 + (e >> 3), lane8 = e & 7;
+        const float* src = P.ss_in + P.ss_row0 + r;
+        float part = 0.f;
+#pragma unroll 4
+        for (int p = lane8; p < P.ss_parts; p += 8) part += __ldcg(src + static_cast<size_t>(p) * P.ss_stride);
+        part += __shfl_down_sync(0xffffffffu, part, 4, 8);
+        part += __shfl_down_sync(0xffffffffu, part, 2, 8);
+        part += __shfl_down_sync(0xffffffffu, part, 1, 8);
+        if (lane8 == 0) s_inv[r] = rsqrtf(part / static_cast<float>(P.H) + P.eps);
       }
     }
     for (int r = e; r < C::ROWS; r += 128) {
@@ -454,6 +491,13 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
     int lt = 0;
     for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
       const int acc = lt & 1;
+      float xpre[16];
+      if (NB == 1 && P.op == OP_RESID) {   // the residual this tile will update, read ahead
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          xpre[j] = (P.grow0 + j < P.n_valid) ? __ldcg(P.y + static_cast<size_t>(P.grow0 + j) * P.y_ld + t * 128 + m)
+                                               : 0.f;
+      }
       if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
       named_bar_sync(1, 128);
       if (!s_misc[1 + acc]) {
@@ -472,7 +516,7 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
           }
-          epilogue_apply<NB>(P, t, ch, v, m, e, xch, xchi, s_inv, s_bv, s_bi);
+          epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
         }
       } else {
         const int slot = part_slot(c, t, U, G, P.KB);
@@ -500,12 +544,24 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            for (int cc = ca; cc <= cb; ++cc) {
-              const float* src = P.part + static_cast<size_t>(part_slot(cc, t, U, G, P.KB)) * C::ROWS * 128;
+            for (int cc = ca; cc <= cb; cc += 2) {   // two segments' loads in flight per round
+              const float* s0 = P.part + static_cast<size_t>(part_slot(cc, t, U, G, P.KB)) * C::ROWS * 128;
+              float a[16], b[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (ch * 16 + j) * 128 + m);
+              for (int j = 0; j < 16; ++j) a[j] = __ldcg(s0 + (ch * 16 + j) * 128 + m);
+              if (cc + 1 <= cb) {
+                const float* s1 = P.part + static_cast<size_t>(part_slot(cc + 1, t, U, G, P.KB)) * C::ROWS * 128;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) b[j] = __ldcg(s1 + (ch * 16 + j) * 128 + m);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += a[j];
+              if (cc + 1 <= cb) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += b[j];
+              }
             }
-            epilogue_apply<NB>(P, t, ch, v, m, e, xch, xchi, s_inv, s_bv, s_bi);
+            epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
           }
         }
       }
@@ -533,16 +589,24 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
         __threadfence();
         if (P.op == OP_LMHEAD) {
           const int B = P.rows_per_seq;
-          for (int r = e; r < C::ROWS; r += 128) {
+          for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
+            const int r = r0 + (e >> 3), lane8 = e & 7;
             float bv = -INFINITY;
             int bi = 0x7fffffff;
-            for (int cc = 0; cc < G; ++cc) {
+#pragma unroll 4
+            for (int cc = lane8; cc < G; cc += 8) {
               const float ov = __ldcg(P.best_v + cc * kMaxPassRows + r);
               const int oi = __ldcg(P.best_i + cc * kMaxPassRows + r);
               if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
             }
+#pragma unroll
+            for (int off = 4; off >= 1; off >>= 1) {
+              const float ov = __shfl_down_sync(0xffffffffu, bv, off, 8);
+              const int oi = __shfl_down_sync(0xffffffffu, bi, off, 8);
+              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
             const int gr = P.grow0 + r;
-            if (gr < P.n_valid) {
+            if (lane8 == 0 && gr < P.n_valid) {
               const int s = gr / B, i = gr - s * B;
               if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
             }
@@ -563,51 +627,64 @@ __global__ void __launch_bounds__(192, 1) gemv_kernel(const __grid_constant__ Ge
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int NB>
-static int launch_nb(const GemvParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
+template <class C>
+static int launch_cfg(const GemvParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = GemvCfg<NB>::SMEM;
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return static_cast<int>(cudaLaunchKernelEx(&cfg, gemv_kernel<NB>, p));
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, gemv_kernel<C>, p));
 }
 
-int gemv_smem_bytes(int nb) {
-  switch (nb) {
-    case 1: return GemvCfg<1>::SMEM;
-    case 2: return GemvCfg<2>::SMEM;
-    case 4: return GemvCfg<4>::SMEM;
-    case 8: return GemvCfg<8>::SMEM;
-    case 16: return GemvCfg<16>::SMEM;
-  }
-  return -1;
+template <class C>
+static int set_attr() {
+  return static_cast<int>(cudaFuncSetAttribute(gemv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+}
+
+// Kernel variants: row groups NB, k-boxes per stage, ring depth, CTAs per SM.
+#define DFL_GEMV_VARIANTS(X)   \
+  X(0, 1, 1, 5, 2)              \
+  X(1, 1, 1, 11, 1)             \
+  X(2, 1, 2, 5, 1)              \
+  X(3, 1, 4, 2, 1)              \
+  X(4, 1, 4, 3, 1)              \
+  X(5, 1, 2, 2, 2)              \
+  X(6, 2, 1, 4, 2)              \
+  X(7, 4, 1, 3, 2)              \
+  X(8, 8, 1, 3, 2)              \
+  X(9, 16, 1, 2, 2)
+
+int gemv_variant(int nb, int pref) {
+  if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 0;
+  return nb == 2 ? 6 : nb == 4 ? 7 : nb == 8 ? 8 : 9;
+}
+
+int gemv_variant_ksub(int v) {
+#define DFL_KS(ID, NB, KS, ST, MB) if (v == ID) return KS;
+  DFL_GEMV_VARIANTS(DFL_KS)
+#undef DFL_KS
+  return 1;
 }
 
 int gemv_set_attributes() {
-  cudaError_t e = cudaSuccess;
-#define DFL_ATTR(NB)                                                                              \
-  if (e == cudaSuccess)                                                                           \
-    e = cudaFuncSetAttribute(gemv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
-                             GemvCfg<NB>::SMEM);
-  DFL_ATTR(1) DFL_ATTR(2) DFL_ATTR(4) DFL_ATTR(8) DFL_ATTR(16)
-#undef DFL_ATTR
-  return static_cast<int>(e);
+  int e = 0;
+#define DFL_SET(ID, NB, KS, ST, MB) if (e == 0) e = set_attr<GemvCfg<NB, KS, ST, MB>>();
+  DFL_GEMV_VARIANTS(DFL_SET)
+#undef DFL_SET
+  return e;
 }
 
-int launch_gemv(const GemvParams& p, int nb, int n_ctas, cudaStream_t stream, bool pdl) {
-  switch (nb) {
-    case 1: return launch_nb<1>(p, n_ctas, stream, pdl);
-    case 2: return launch_nb<2>(p, n_ctas, stream, pdl);
-    case 4: return launch_nb<4>(p, n_ctas, stream, pdl);
-    case 8: return launch_nb<8>(p, n_ctas, stream, pdl);
-    case 16: return launch_nb<16>(p, n_ctas, stream, pdl);
-  }
+int launch_gemv(const GemvParams& p, int variant, int n_ctas, cudaStream_t stream, bool pdl) {
+#define DFL_LAUNCH(ID, NB, KS, ST, MB) \
+  if (variant == ID) return launch_cfg<GemvCfg<NB, KS, ST, MB>>(p, n_ctas, stream, pdl);
+  DFL_GEMV_VARIANTS(DFL_LAUNCH)
+#undef DFL_LAUNCH
   return static_cast<int>(cudaErrorInvalidValue);
 }
 

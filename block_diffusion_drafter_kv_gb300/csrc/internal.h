@@ -84,9 +84,11 @@ struct GemvParams {
   int* drafted;
 };
 
-// NB = activation row groups of 16 (1, 2, 4, 8 or 16). Returns cudaError_t.
-int launch_gemv(const GemvParams& p, int nb, int n_ctas, cudaStream_t stream, bool pdl);
-int gemv_smem_bytes(int nb);
+// Kernel variant for nb activation row groups of 16 (1, 2, 4, 8 or 16); `pref` selects
+// among the nb == 1 variants. KB of a launch counts k-stages of 64 * gemv_variant_ksub(v).
+int gemv_variant(int nb, int pref);
+int gemv_variant_ksub(int variant);
+int launch_gemv(const GemvParams& p, int variant, int n_ctas, cudaStream_t stream, bool pdl);
 int gemv_set_attributes();
 
 // ---------------------------------------------------------------- block attention

@@ -9,9 +9,12 @@ namespace dfl {
 // mask embedding (jansverre.net, "Hva gjør DFlash annerledes ...": the drafter denoises a
 // masked token block). Writes the fp32 residual x, its bf16 copy scaled by layer 0's
 // attention-norm gain (the next projection's operand) and each row's sum of squares.
+// All loads of a thread are issued before any of its stores (the buffers could alias as far
+// as the compiler knows), so the kernel costs one memory round trip, not one per element.
 __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int kMaxIter = 4;  // H <= 4 * 8 * blockDim
   const int row = blockIdx.x;
   const int s = row / P.B, i = row - s * P.B;
   const __nv_bfloat16* src = P.mask_emb;
@@ -24,14 +27,38 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
     src = P.embed + static_cast<size_t>(tok) * P.H;
     if (threadIdx.x == 0 && __ldcg(P.len + s) + P.B > P.cap) raise_flag(P.err, kDevCapacity);
   }
+  uint4 xs[kMaxIter], gs[kMaxIter];
+#pragma unroll
+  for (int it = 0; it < kMaxIter; ++it) {
+    const int f0 = (it * blockDim.x + threadIdx.x) * 8;
+    if (f0 < P.H) {
+      xs[it] = *reinterpret_cast<const uint4*>(src + f0);
+      gs[it] = *reinterpret_cast<const uint4*>(P.gain + f0);
+    }
+  }
   float ss = 0.f;
-  for (int f = threadIdx.x; f < P.H; f += blockDim.x) {
-    const float x = __bfloat162float(src[f]);
-    const size_t off = static_cast<size_t>(row) * P.H + f;
-    P.x[off] = x;
-    P.xg[off] = __float2bfloat16_rn(x * __bfloat162float(P.gain[f]));
-    if (P.trace) P.trace[off] = x;
-    ss += x * x;
+#pragma unroll
+  for (int it = 0; it < kMaxIter; ++it) {
+    const int f0 = (it * blockDim.x + threadIdx.x) * 8;
+    if (f0 >= P.H) continue;
+    const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(&xs[it]);
+    const __nv_bfloat16* gv = reinterpret_cast<const __nv_bfloat16*>(&gs[it]);
+    float x[8];
+    __nv_bfloat16 xg[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      x[k] = __bfloat162float(xv[k]);
+      xg[k] = __float2bfloat16_rn(x[k] * __bfloat162float(gv[k]));
+      ss += x[k] * x[k];
+    }
+    const size_t off = static_cast<size_t>(row) * P.H + f0;
+    *reinterpret_cast<float4*>(P.x + off) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(P.x + off + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    *reinterpret_cast<uint4*>(P.xg + off) = *reinterpret_cast<const uint4*>(xg);
+    if (P.trace) {
+      *reinterpret_cast<float4*>(P.trace + off) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(P.trace + off + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
   }
   __shared__ float red[8];
 #pragma unroll
@@ -82,12 +109,24 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   if ((V & 3) == 0) {
-    for (int k = c0 + 4 * static_cast<int>(threadIdx.x); k < c1; k += 4 * blockDim.x) {
-      const float4 q = __ldcs(reinterpret_cast<const float4*>(row + k));
-      better(bv, bi, q.x, k);
-      better(bv, bi, q.y, k + 1);
-      better(bv, bi, q.z, k + 2);
-      better(bv, bi, q.w, k + 3);
+    constexpr int U = 8;  // float4 loads in flight per thread before any compare
+    const int stride = 4 * blockDim.x;
+    for (int base = c0 + 4 * static_cast<int>(threadIdx.x); base < c1; base += U * stride) {
+      float4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = base + u * stride;
+        q[u] = k < c1 ? __ldcs(reinterpret_cast<const float4*>(row + k))
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = base + u * stride;
+        better(bv, bi, q[u].x, k);
+        better(bv, bi, q[u].y, k + 1);
+        better(bv, bi, q[u].z, k + 2);
+        better(bv, bi, q[u].w, k + 3);
+      }
     }
   } else {
     for (int k = c0 + static_cast<int>(threadIdx.x); k < c1; k += blockDim.x) better(bv, bi, __ldcs(row + k), k);
@@ -120,14 +159,23 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (threadIdx.x < B) {
+  {  // row argmax over the chunks: 16 lanes per row, all loads in flight, then a lane tree
+    const int r = threadIdx.x >> 4, l16 = threadIdx.x & 15;
     float v = -INFINITY;
     int idx = 0x7fffffff;
-    for (int c = 0; c < P.chunks; ++c) {
-      const int slot = (s * B + threadIdx.x) * P.chunks + c;
-      better(v, idx, __ldcg(P.part_v + slot), __ldcg(P.part_i + slot));
+    if (r < B) {
+      for (int c = l16; c < P.chunks; c += 16) {
+        const int slot = (s * B + r) * P.chunks + c;
+        better(v, idx, __ldcg(P.part_v + slot), __ldcg(P.part_i + slot));
+      }
     }
-    g[threadIdx.x] = idx;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {   // every lane of the warp takes part
+      const float ov = __shfl_down_sync(0xffffffffu, v, o, 16);
+      const int oi = __shfl_down_sync(0xffffffffu, idx, o, 16);
+      better(v, idx, ov, oi);
+    }
+    if (r < B && l16 == 0) g[r] = idx;
   }
   __syncthreads();
   if (threadIdx.x == 0) {

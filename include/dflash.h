@@ -60,7 +60,7 @@ extern "C" {
 
 /* ---- drafter shape ---------------------------------------------------------------- */
 typedef struct dflash_config {
-  int32_t hidden;        /* H: drafter hidden size, multiple of 128 */
+  int32_t hidden;        /* H: drafter hidden size, multiple of 128, at most 8192 */
   int32_t n_heads;       /* nq: query heads */
   int32_t n_kv_heads;    /* nkv: key/value heads; nq % nkv == 0, nq/nkv <= 8 */
   int32_t head_dim;      /* d: 64 or 128; nq*d and nkv*d multiples of 128 */
