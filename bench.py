@@ -62,25 +62,24 @@ def peaks():
 
 # ------------------------------------------------------------------ algorithmic traffic
 
-def gemv_launches(s, batch, B, tau):
-    """(label, bytes, flops) of every weight-streaming launch of one step, in launch order.
-    Bytes: the weight read once, the activation rows read once, the outputs written once."""
+def proj_bytes_flops(s, batch, B, tau):
+    """Algorithmic (bytes, flops) of each projection: the weight read once, the activation
+    rows read once, the outputs written once."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     rows = batch * B
-    out = []
     kin = s.n_taps * s.target_hidden
-    out.append(("fc", 2 * H * kin + 2 * tau * kin + 2 * tau * H, 2 * tau * H * kin))
     kv = 2 * s.n_layers * s.n_kv_heads * d
-    out.append(("kv", 2 * kv * H + 2 * tau * H + 2 * tau * kv, 2 * tau * kv * H))
-    for _ in range(s.n_layers):
-        nqkv = (s.n_heads + 2 * s.n_kv_heads) * d
-        out.append(("qkv", 2 * nqkv * H + 2 * rows * (H + nqkv), 2 * rows * nqkv * H))
-        out.append(("attn", None, None))
-        out.append(("o", 2 * H * s.n_heads * d + 2 * rows * s.n_heads * d + 4 * 2 * rows * H, 2 * rows * H * s.n_heads * d))
-        out.append(("gateup", 2 * 2 * I * H + 2 * rows * (H + I), 2 * rows * 2 * I * H))
-        out.append(("down", 2 * H * I + 2 * rows * I + 4 * 2 * rows * H, 2 * rows * H * I))
-    out.append(("lm_head", 2 * V * H + 2 * rows * H + 4 * batch * (B - 1), 2 * batch * (B - 1) * V * H))
-    return out
+    nqkv = (s.n_heads + 2 * s.n_kv_heads) * d
+    nqd = s.n_heads * d
+    return {
+        "fc": (2 * H * kin + 2 * tau * kin + 2 * tau * H, 2 * tau * H * kin),
+        "kv": (2 * kv * H + 2 * tau * H + 2 * tau * kv, 2 * tau * kv * H),
+        "qkv": (2 * nqkv * H + 2 * rows * (H + nqkv), 2 * rows * nqkv * H),
+        "o": (2 * H * nqd + 2 * rows * nqd + 4 * 2 * rows * H, 2 * rows * H * nqd),
+        "gateup": (2 * 2 * I * H + 2 * rows * (H + I), 2 * rows * 2 * I * H),
+        "down": (2 * H * I + 2 * rows * I + 4 * 2 * rows * H, 2 * rows * H * I),
+        "lm_head": (2 * V * H + 2 * rows * H + 4 * batch * (B - 1), 2 * batch * (B - 1) * V * H),
+    }
 
 
 def attn_bytes_flops(s, batch, B, n_ctx):
@@ -91,15 +90,33 @@ def attn_bytes_flops(s, batch, B, n_ctx):
     return kvb + qo, fl
 
 
+def launch_plan(s, batch, B, tau, n_ctx):
+    """Launch order of one step by call: (label, kind, bytes, flops). kind "gemv" marks the
+    weight-streaming kernel (one launch runs a chain of projections)."""
+    pj = proj_bytes_flops(s, batch, B, tau)
+    add = lambda *ks: tuple(map(sum, zip(*[pj[k] for k in ks])))
+    ab = attn_bytes_flops(s, batch, B, n_ctx)
+    draft = [("embed", "small", 2 * s.hidden * batch * (1 + 6 * B), 0), ("qkv", "gemv", *pj["qkv"])]
+    for l in range(s.n_layers):
+        last = l == s.n_layers - 1
+        draft.append(("attn", "attn", *ab))
+        if last:
+            draft.append(("o+gateup+down+lm_head", "gemv", *add("o", "gateup", "down", "lm_head")))
+        else:
+            draft.append(("o+gateup+down+qkv", "gemv", *add("o", "gateup", "down", "qkv")))
+    return {
+        "inject": [("fc+kv", "gemv", *add("fc", "kv"))],
+        "draft": draft,
+        "verify": [("verify", "small", 4 * batch * B * s.vocab, 0)],
+    }
+
+
 def step_bytes_flops(s, batch, B, n_ctx, tau):
     byt = fl = 0
-    for lab, b, f in gemv_launches(s, batch, B, tau):
-        if lab == "attn":
-            b, f = attn_bytes_flops(s, batch, B, n_ctx)
-        byt += b
-        fl += f
-    byt += 2 * s.hidden * batch                           # embedding rows
-    byt += 4 * batch * B * s.vocab                        # target logits read by verify
+    for call in launch_plan(s, batch, B, tau, n_ctx).values():
+        for _, kind, b, f in call:
+            byt += b
+            fl += f
     return byt, fl
 
 
@@ -386,58 +403,47 @@ def run_cuda(a):
             ev.record(stream)
         stream.synchronize()
         dr.trace_events(evs)
-        labels_inj = ["fc", "kv"]
-        labels_dr = ["embed"] + ["qkv", "attn", "o", "gateup", "down"] * s.n_layers + ["lm_head"]
+        plan = launch_plan(s, batch, B, tau_avg, n_avg)
         with torch.cuda.stream(stream):
             reset()
         stream.synchronize()
         acc_t = {}
 
-        def collect(labels, n):
+        def collect(call, n):
             torch.cuda.synchronize()
-            for i in range(min(n, len(labels))):
-                acc_t.setdefault(labels[i], []).append(evs[i].elapsed_time(evs[i + 1]))
+            assert n == len(plan[call]), f"{call}: {n} launches, plan has {len(plan[call])}"
+            for i, (lab, kind, b, f) in enumerate(plan[call]):
+                acc_t.setdefault((lab, kind, b), []).append(evs[i].elapsed_time(evs[i + 1]))
 
         for _ in range(a.trace_steps):
-            n_ctx_now = float(dr.len[:batch].float().mean())
-            tau_now = float(accept[:batch].float().mean())
             with torch.cuda.stream(stream):
                 dr.inject(hid_step, B, accept, batch)
-            collect(labels_inj, dr.last_launch_count())
+            collect("inject", dr.last_launch_count())
             with torch.cuda.stream(stream):
                 dr.draft(batch, B, drafted)
-            collect(labels_dr, dr.last_launch_count())
+            collect("draft", dr.last_launch_count())
             with torch.cuda.stream(stream):
                 BND.synth_plant(noise, drafted, masks, n_masks, step_ctr, batch, B, 10.0, saved)
                 dr.verify(noise, drafted, batch, B, accept, committed)
-            collect(["verify"], dr.last_launch_count())
+            collect("verify", dr.last_launch_count())
             with torch.cuda.stream(stream):
                 BND.synth_unplant(noise, step_ctr, n_masks, batch, B, saved)
         dr.trace_events([])
         stream.synchronize()
-        gl = gemv_launches(s, batch, B, tau_avg)
-        gbytes = {}
-        for lab, b, f in gl:
-            if b is not None:
-                gbytes.setdefault(lab, []).append(b)
-        ab, af = attn_bytes_flops(s, batch, B, n_avg)
         sum_b = sum_t = 0.0
-        for lab, ts in acc_t.items():
-            per_step_launches_lab = labels_inj.count(lab) + labels_dr.count(lab) + (lab == "verify")
+        for (lab, kind, b), ts in acc_t.items():
             us = 1e3 * sum(ts) / len(ts)
-            bb = None
-            if lab in gbytes:
-                bb = gbytes[lab][0]
-                sum_b += bb * len(ts)
+            k = kern.setdefault(lab, {"us": 0.0, "launches_per_step": 0, "bytes": 0})
+            n_per = len(ts) // a.trace_steps
+            k["us"] = round((k["us"] * k["launches_per_step"] + us * n_per) / (k["launches_per_step"] + n_per), 2)
+            k["launches_per_step"] += n_per
+            k["bytes"] = b
+            k["gbs"] = round(b / (k["us"] * 1e-6) / 1e9, 1) if b else None
+            if kind == "gemv":
+                sum_b += b * len(ts)
                 sum_t += sum(ts) * 1e-3
-            elif lab == "attn":
-                bb = ab
-            elif lab == "verify":
-                bb = 4 * batch * B * s.vocab
-            kern[lab] = {"us": round(us, 2), "launches_per_step": per_step_launches_lab,
-                         "gbs": round(bb / (us * 1e-6) / 1e9, 1) if bb else None}
         achieved = sum_b / sum_t / 1e9
-        roof = {"bound": "hbm", "kernel": "gemv_kernel (weight-streaming tcgen05 GEMM, all projections)",
+        roof = {"bound": "hbm", "kernel": "gemv_kernel (weight-streaming tcgen05 GEMM chains, all projections)",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "traffic": None, "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)",
                 "timing": "per-launch CUDA events on the launching stream, launches serialised"}

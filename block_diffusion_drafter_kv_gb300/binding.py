@@ -51,6 +51,8 @@ SIGNATURES = {
     "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32]),
     "dflash_last_launch_count": (c_int32, [c_void_p]),
     "dflash_trace_events": (c_int32, [c_void_p, POINTER(c_void_p), c_int32]),
+    "dflash_timeline": (c_int32, [c_void_p, c_void_p, ctypes.c_int64]),
+    "dflash_timeline_used": (ctypes.c_int64, [c_void_p]),
     "dflash_status_string": (ctypes.c_char_p, [c_int32]),
     "dflash_verify_greedy_noalloc": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p,
                                                c_void_p, c_void_p]),
@@ -172,6 +174,15 @@ class Drafter:
 
     def last_launch_count(self) -> int:
         return self.L.dflash_last_launch_count(self.h)
+
+    def timeline(self, records=None) -> None:
+        """Per-CTA timeline into `records` (int64 CUDA tensor [n, 21]); None turns it off."""
+        n = 0 if records is None else records.shape[0]
+        self._tl_keep = records
+        check(self.L.dflash_timeline(self.h, None if records is None else records.data_ptr(), n), "dflash_timeline")
+
+    def timeline_used(self) -> int:
+        return self.L.dflash_timeline_used(self.h)
 
     def trace_events(self, events) -> None:
         """Record torch.cuda.Event objects around each launch of later calls ([] turns it off)."""

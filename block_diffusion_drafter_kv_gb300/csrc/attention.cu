@@ -56,6 +56,12 @@ DEV uint32_t kv_addr(uint32_t base, int key, int d) {
 
 template <int D>
 __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnParams P) {
+  unsigned long long* tl = P.tl ? P.tl + static_cast<size_t>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kTlWords : nullptr;
+  if (tl && threadIdx.x == 0) {
+    tl[0] = (static_cast<unsigned long long>(TL_ATTN) << 32) | static_cast<unsigned>(P.tl_id);
+    tl[1] = smid();
+    tl_stamp(tl, 2);
+  }
   constexpr int TILE_BYTES = KT * D * 2;
   constexpr int NBOX = D / 64;
   constexpr int NT_D = D / 8;   // n-tiles over d in the output
@@ -122,6 +128,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   }
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0) tl_stamp(tl, 5);
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_last();
     for (int i = 0; i < pre; ++i)
@@ -308,6 +315,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     P.o[(static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d] =
         __float2bfloat16_rn(acc);
   }
+  if (threadIdx.x == 0) tl_stamp(tl, 20);
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 

@@ -20,6 +20,7 @@ using namespace dfl;
 namespace {
 
 constexpr int kMaxChunks = 64;   // verification chunks per row
+constexpr int kChainSlots = 64;  // barrier-counter sets, used round robin by consecutive launches
 constexpr int kMaxLayersPerKvLaunch = kMaxAMaps / 2;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -27,7 +28,7 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 struct WsLayout {
   size_t err, tile_cnt, cta_cnt, seq_cnt, rope_cos, rope_sin, part, best_v, best_i;
-  size_t ss_fc, ss_x, ss_emb, cfeat, x, xg, q, o, act, vpart_v, vpart_i, plant;
+  size_t ss_fc, ss_x, ss_emb, cfeat, x, xg, q, o, act, vpart_v, vpart_i, chain_bar;
   size_t total;
   int R;          // draft rows allocated (multiple of 16)
   int max_tiles;  // tile counters
@@ -75,6 +76,7 @@ WsLayout layout_of(const dflash_config& c) {
   L.act = take(R * I * 2);
   L.vpart_v = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
   L.vpart_i = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
+  L.chain_bar = take(static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4);
   L.total = off;
   return L;
 }
@@ -146,6 +148,7 @@ struct dflash_handle {
   int n_sms = 0;
   int inject_pass_rows = 16;
   int gemv_pref = 2;  // weight-streaming kernel variant for single-row-group launches
+  int chain_slot = 0;
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -161,6 +164,9 @@ struct dflash_handle {
   std::vector<CUtensorMap> m_kcache, m_vcache;
   int last_launches = 0;
   std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
+  unsigned long long* tl_buf = nullptr;  // caller-owned timeline buffer, or null
+  long long tl_cap = 0, tl_next = 0;     // records
+  int tl_launch = 0;
 
   template <typename T>
   T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -179,6 +185,14 @@ void gemv_common(const dflash_handle* h, GemvParams& P) {
   P.n_out = 0x7fffffff;
 }
 
+// Timeline records for a launch of n CTAs (null when the timeline is off or full).
+unsigned long long* tl_take(dflash_handle* h, long long n) {
+  if (!h->tl_buf || h->tl_next + n > h->tl_cap) return nullptr;
+  unsigned long long* p = h->tl_buf + h->tl_next * kTlWords;
+  h->tl_next += n;
+  return p;
+}
+
 // Start of a call: reset the launch count; with tracing on, record event 0.
 void call_begin(dflash_handle* h, cudaStream_t st) {
   h->last_launches = 0;
@@ -191,22 +205,35 @@ void note_launch(dflash_handle* h, cudaStream_t st) {
   if (h->last_launches < static_cast<int>(h->trace_ev.size())) cudaEventRecord(h->trace_ev[h->last_launches], st);
 }
 
-// P.KB arrives in 64-wide k-blocks; the chosen kernel variant may stage several per step.
-int run_gemv(dflash_handle* h, const GemvParams& P0, int nb, cudaStream_t st) {
-  GemvParams P = P0;
+// One persistent launch over a chain of projection phases (all with nb row groups). Each
+// phase's KB arrives in 64-wide k-blocks; the kernel variant may stage several per step.
+int run_chain(dflash_handle* h, const GemvParams* phases, int n, int nb, cudaStream_t st) {
+  GemvChain C{};
   int v = gemv_variant(nb, h->gemv_pref);
   int ks = gemv_variant_ksub(v);
-  if (P.KB % ks != 0) {
-    v = gemv_variant(nb, 0);
-    ks = gemv_variant_ksub(v);
+  for (int p = 0; p < n; ++p)
+    if (phases[p].KB % ks != 0) {
+      v = gemv_variant(nb, 0);
+      ks = gemv_variant_ksub(v);
+    }
+  for (int p = 0; p < n; ++p) {
+    C.ph[p] = phases[p];
+    C.ph[p].KB /= ks;
   }
-  P.KB /= ks;
-  const long long U = static_cast<long long>(P.T) * P.KB;
-  const int G = static_cast<int>(std::min<long long>(std::min(h->n_sms, kMaxCtas), U));
-  const int e = launch_gemv(P, v, G, st, h->trace_ev.empty());
+  C.n_phases = n;
+  const int slot = h->chain_slot;
+  h->chain_slot = (h->chain_slot + 1) % kChainSlots;
+  C.bar = h->at<int>(h->L.chain_bar) + slot * (kMaxPhases + 4);
+  C.exit_cnt = C.bar + kMaxPhases;
+  const int G = std::min(h->n_sms, kMaxCtas);
+  C.tl = tl_take(h, G);
+  C.tl_id = h->tl_launch++;
+  const int e = launch_gemv(C, v, G, st, h->trace_ev.empty());
   note_launch(h, st);
   return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
 }
+
+int run_gemv(dflash_handle* h, const GemvParams& P, int nb, cudaStream_t st) { return run_chain(h, &P, 1, nb, st); }
 
 #define DFL_TRY(x)                \
   do {                            \
@@ -362,8 +389,10 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
   const int tkv = c.n_kv_heads * d / 128;
   for (int p = 0; p < n_pass; ++p) {
     const int row0 = p * pass_rows;
+    GemvParams ph[kMaxPhases]{};
+    int np = 0;
     {  // context fusion: F = concat(hidden taps) · Wfcᵀ
-      GemvParams P{};
+      GemvParams& P = ph[np++];
       gemv_common(h, P);
       P.amap[0] = h->m_fc;
       P.n_amaps = 1;
@@ -383,11 +412,10 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
       P.yb_ld = H;
       P.ss_out = h->at<float>(h->L.ss_fc);
       P.ss_stride = kMaxPassRows;
-      DFL_TRY(run_gemv(h, P, nb, st));
     }
     for (int l0 = 0; l0 < c.n_layers; l0 += kMaxLayersPerKvLaunch) {  // K/V of every layer
       const int nl = std::min(kMaxLayersPerKvLaunch, c.n_layers - l0);
-      GemvParams P{};
+      GemvParams& P = ph[np++];
       gemv_common(h, P);
       P.n_amaps = 2 * nl;
       for (int i = 0; i < nl; ++i) {
@@ -418,8 +446,8 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
       P.rows_per_seq = rows_per_seq;
       P.batch = batch;
       P.commit_len = (p == n_pass - 1) && (l0 + nl == c.n_layers);
-      DFL_TRY(run_gemv(h, P, nb, st));
     }
+    DFL_TRY(run_chain(h, ph, np, nb, st));
   }
   return DFLASH_OK;
 }
@@ -453,18 +481,13 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     E.H = H;
     E.V = c.vocab;
     E.cap = c.kv_capacity;
+    E.tl = tl_take(h, batch * block);
+    E.tl_id = h->tl_launch++;
     if (launch_embed(E, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
     note_launch(h, st);
   }
-  // rows are processed in passes of at most kMaxPassRows (one MMA N per pass)
-  auto for_passes = [&](auto&& fn) -> int {
-    for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {
-      const int pr = std::min(kMaxPassRows, rows - row0);
-      DFL_TRY(fn(row0, nb_for_rows(pr)));
-    }
-    return DFLASH_OK;
-  };
-  auto base = [&](GemvParams& P, int row0, int nb, const CUtensorMap& bmap) {
+  // Projection phases for a pass of rows [row0, row0 + pass rows).
+  auto base = [&](GemvParams& P, int row0, const CUtensorMap& bmap) {
     gemv_common(h, P);
     P.bmap = bmap;
     P.b_row0 = row0;
@@ -474,142 +497,158 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     P.n_valid = rows;
     P.rows_per_seq = block;
     P.batch = batch;
-    (void)nb;
   };
-  for (int l = 0; l < L; ++l) {
-    DFL_TRY(for_passes([&](int row0, int nb) {  // q, k, v with RoPE; block k/v into the cache
-      GemvParams P{};
-      base(P, row0, nb, h->m_xg[nb_index(nb)]);
-      P.amap[0] = h->m_wq[l];
-      P.amap[1] = h->m_wk[l];
-      P.amap[2] = h->m_wv[l];
-      P.n_amaps = 3;
-      P.tile_start[0] = 0;
-      P.tile_start[1] = tq;
-      P.tile_start[2] = tq + tk;
-      P.tile_start[3] = tq + 2 * tk;
-      P.T = tq + 2 * tk;
-      P.KB = H / 64;
-      P.op = OP_QKV;
-      if (l == 0) {
-        P.ss_in = h->at<float>(h->L.ss_emb);
-        P.ss_parts = 1;
-      } else {
-        P.ss_in = h->at<float>(h->L.ss_x);
-        P.ss_parts = H / 128;
-      }
-      P.ss_stride = R;
-      P.yb = h->at<__nv_bfloat16>(h->L.q);
-      P.yb_ld = c.n_heads * d;
-      P.rope_cos = h->at<float>(h->L.rope_cos);
-      P.rope_sin = h->at<float>(h->L.rope_sin);
-      P.d = d;
-      P.kc = h->kc;
-      P.vc = h->vc;
-      P.nkv = c.n_kv_heads;
-      P.cap = c.kv_capacity;
-      P.max_batch = c.max_batch;
-      P.layer = l;
-      P.len = h->len;
-      return run_gemv(h, P, nb, st);
-    }));
-    {  // bidirectional attention over injected context + block
-      AttnParams A{};
-      A.kmap = h->m_kcache[l];
-      A.vmap = h->m_vcache[l];
-      A.q = h->at<__nv_bfloat16>(h->L.q);
-      A.o = h->at<__nv_bfloat16>(h->L.o);
-      A.len = h->len;
-      A.err = h->at<int>(h->L.err);
-      A.B = block;
-      A.nq = c.n_heads;
-      A.nkv = c.n_kv_heads;
-      A.d = d;
-      A.cap = c.kv_capacity;
-      A.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-      int split = h->n_sms / (batch * c.n_kv_heads);
-      split = std::max(1, std::min(8, split));
-      if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
-      note_launch(h, st);
-    }
-    DFL_TRY(for_passes([&](int row0, int nb) {  // x += o · Woᵀ
-      GemvParams P{};
-      base(P, row0, nb, h->m_o[nb_index(nb)]);
-      P.amap[0] = h->m_wo[l];
-      P.n_amaps = 1;
-      P.tile_start[1] = H / 128;
-      P.T = H / 128;
-      P.KB = c.n_heads * d / 64;
-      P.op = OP_RESID;
-      P.y = h->at<float>(h->L.x);
-      P.y_ld = H;
-      P.yb = h->at<__nv_bfloat16>(h->L.xg);
-      P.yb_ld = H;
-      P.gain = static_cast<const __nv_bfloat16*>(h->layers[l].g_mlp);
-      P.ss_out = h->at<float>(h->L.ss_x);
-      P.ss_stride = R;
-      return run_gemv(h, P, nb, st);
-    }));
-    DFL_TRY(for_passes([&](int row0, int nb) {  // act = silu(gate) * up
-      GemvParams P{};
-      base(P, row0, nb, h->m_xg[nb_index(nb)]);
-      P.amap[0] = h->m_wg[l];
-      P.amap[1] = h->m_wu[l];
-      P.n_amaps = 2;
-      P.pair_mode = 1;
-      P.T = c.intermediate / 64;
-      P.KB = H / 64;
-      P.op = OP_SWIGLU;
+  auto qkv = [&](GemvParams& P, int l, int row0, int nb) {  // q, k, v with RoPE; block k/v into the cache
+    base(P, row0, h->m_xg[nb_index(nb)]);
+    P.amap[0] = h->m_wq[l];
+    P.amap[1] = h->m_wk[l];
+    P.amap[2] = h->m_wv[l];
+    P.n_amaps = 3;
+    P.tile_start[0] = 0;
+    P.tile_start[1] = tq;
+    P.tile_start[2] = tq + tk;
+    P.tile_start[3] = tq + 2 * tk;
+    P.T = tq + 2 * tk;
+    P.KB = H / 64;
+    P.op = OP_QKV;
+    if (l == 0) {
+      P.ss_in = h->at<float>(h->L.ss_emb);
+      P.ss_parts = 1;
+    } else {
       P.ss_in = h->at<float>(h->L.ss_x);
       P.ss_parts = H / 128;
-      P.ss_stride = R;
-      P.yb = h->at<__nv_bfloat16>(h->L.act);
-      P.yb_ld = c.intermediate;
-      return run_gemv(h, P, nb, st);
-    }));
-    DFL_TRY(for_passes([&](int row0, int nb) {  // x += act · W_downᵀ
-      GemvParams P{};
-      base(P, row0, nb, h->m_act[nb_index(nb)]);
-      P.amap[0] = h->m_wd[l];
-      P.n_amaps = 1;
-      P.tile_start[1] = H / 128;
-      P.T = H / 128;
-      P.KB = c.intermediate / 64;
-      P.op = OP_RESID;
-      P.y = h->at<float>(h->L.x);
-      P.y_ld = H;
-      P.yb = h->at<__nv_bfloat16>(h->L.xg);
-      P.yb_ld = H;
-      P.gain = static_cast<const __nv_bfloat16*>(l + 1 < L ? h->layers[l + 1].g_attn : h->w.g_final);
-      P.ss_out = h->at<float>(h->L.ss_x);
-      P.ss_stride = R;
-      P.trace = x_trace ? x_trace + static_cast<size_t>(l + 1) * rows * H : nullptr;
-      return run_gemv(h, P, nb, st);
+    }
+    P.ss_stride = R;
+    P.yb = h->at<__nv_bfloat16>(h->L.q);
+    P.yb_ld = c.n_heads * d;
+    P.rope_cos = h->at<float>(h->L.rope_cos);
+    P.rope_sin = h->at<float>(h->L.rope_sin);
+    P.d = d;
+    P.kc = h->kc;
+    P.vc = h->vc;
+    P.nkv = c.n_kv_heads;
+    P.cap = c.kv_capacity;
+    P.max_batch = c.max_batch;
+    P.layer = l;
+    P.len = h->len;
+  };
+  auto oproj = [&](GemvParams& P, int l, int row0, int nb) {  // x += o · Woᵀ
+    base(P, row0, h->m_o[nb_index(nb)]);
+    P.amap[0] = h->m_wo[l];
+    P.n_amaps = 1;
+    P.tile_start[1] = H / 128;
+    P.T = H / 128;
+    P.KB = c.n_heads * d / 64;
+    P.op = OP_RESID;
+    P.y = h->at<float>(h->L.x);
+    P.y_ld = H;
+    P.yb = h->at<__nv_bfloat16>(h->L.xg);
+    P.yb_ld = H;
+    P.gain = static_cast<const __nv_bfloat16*>(h->layers[l].g_mlp);
+    P.ss_out = h->at<float>(h->L.ss_x);
+    P.ss_stride = R;
+  };
+  auto gateup = [&](GemvParams& P, int l, int row0, int nb) {  // act = silu(gate) * up
+    base(P, row0, h->m_xg[nb_index(nb)]);
+    P.amap[0] = h->m_wg[l];
+    P.amap[1] = h->m_wu[l];
+    P.n_amaps = 2;
+    P.pair_mode = 1;
+    P.T = c.intermediate / 64;
+    P.KB = H / 64;
+    P.op = OP_SWIGLU;
+    P.ss_in = h->at<float>(h->L.ss_x);
+    P.ss_parts = H / 128;
+    P.ss_stride = R;
+    P.yb = h->at<__nv_bfloat16>(h->L.act);
+    P.yb_ld = c.intermediate;
+  };
+  auto down = [&](GemvParams& P, int l, int row0, int nb) {  // x += act · W_downᵀ
+    base(P, row0, h->m_act[nb_index(nb)]);
+    P.amap[0] = h->m_wd[l];
+    P.n_amaps = 1;
+    P.tile_start[1] = H / 128;
+    P.T = H / 128;
+    P.KB = c.intermediate / 64;
+    P.op = OP_RESID;
+    P.y = h->at<float>(h->L.x);
+    P.y_ld = H;
+    P.yb = h->at<__nv_bfloat16>(h->L.xg);
+    P.yb_ld = H;
+    P.gain = static_cast<const __nv_bfloat16*>(l + 1 < L ? h->layers[l + 1].g_attn : h->w.g_final);
+    P.ss_out = h->at<float>(h->L.ss_x);
+    P.ss_stride = R;
+    P.trace = x_trace ? x_trace + static_cast<size_t>(l + 1) * rows * H : nullptr;
+  };
+  auto lmhead = [&](GemvParams& P, int row0, int nb) {  // final norm, LM head, argmax
+    base(P, row0, h->m_xg[nb_index(nb)]);
+    P.amap[0] = h->m_lm;
+    P.n_amaps = 1;
+    P.T = ceil_div(c.vocab, 128);
+    P.tile_start[1] = P.T;
+    P.KB = H / 64;
+    P.op = OP_LMHEAD;
+    P.ss_in = h->at<float>(h->L.ss_x);
+    P.ss_parts = H / 128;
+    P.ss_stride = R;
+    P.logits = logits;
+    P.vocab = c.vocab;
+    P.n_out = c.vocab;
+    P.best_v = h->at<float>(h->L.best_v);
+    P.best_i = h->at<int>(h->L.best_i);
+    P.drafted = drafted;
+  };
+  // Rows are processed in passes of at most kMaxPassRows (one MMA N per pass); each pass
+  // runs its chain of projections independently (rows do not interact outside attention).
+  auto chain_passes = [&](auto&& build) -> int {
+    for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {
+      const int nb = nb_for_rows(std::min(kMaxPassRows, rows - row0));
+      GemvParams ph[kMaxPhases]{};
+      const int np = build(ph, row0, nb);
+      if (np > 0) DFL_TRY(run_chain(h, ph, np, nb, st));
+    }
+    return DFLASH_OK;
+  };
+  auto attention = [&](int l) -> int {  // bidirectional attention over injected context + block
+    AttnParams A{};
+    A.kmap = h->m_kcache[l];
+    A.vmap = h->m_vcache[l];
+    A.q = h->at<__nv_bfloat16>(h->L.q);
+    A.o = h->at<__nv_bfloat16>(h->L.o);
+    A.len = h->len;
+    A.err = h->at<int>(h->L.err);
+    A.B = block;
+    A.nq = c.n_heads;
+    A.nkv = c.n_kv_heads;
+    A.d = d;
+    A.cap = c.kv_capacity;
+    A.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    int split = h->n_sms / (batch * c.n_kv_heads);
+    split = std::max(1, std::min(8, split));
+    A.tl = tl_take(h, static_cast<long long>(split) * c.n_kv_heads * batch);
+    A.tl_id = h->tl_launch++;
+    if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+    note_launch(h, st);
+    return DFLASH_OK;
+  };
+  // chain sequence: [qkv 0] attn 0 [o 0, gate/up 0, down 0, qkv 1] attn 1 ... [o L-1, ..., LM head]
+  DFL_TRY(chain_passes([&](GemvParams* ph, int row0, int nb) {
+    qkv(ph[0], 0, row0, nb);
+    return 1;
+  }));
+  for (int l = 0; l < L; ++l) {
+    DFL_TRY(attention(l));
+    DFL_TRY(chain_passes([&](GemvParams* ph, int row0, int nb) {
+      int np = 0;
+      oproj(ph[np++], l, row0, nb);
+      gateup(ph[np++], l, row0, nb);
+      down(ph[np++], l, row0, nb);
+      if (l + 1 < L) qkv(ph[np++], l + 1, row0, nb);
+      else if (block > 1) lmhead(ph[np++], row0, nb);
+      return np;
     }));
   }
   (void)layer_elems;
-  if (block > 1) {
-    DFL_TRY(for_passes([&](int row0, int nb) {  // final norm, LM head, argmax
-      GemvParams P{};
-      base(P, row0, nb, h->m_xg[nb_index(nb)]);
-      P.amap[0] = h->m_lm;
-      P.n_amaps = 1;
-      P.T = ceil_div(c.vocab, 128);
-      P.tile_start[1] = P.T;
-      P.KB = H / 64;
-      P.op = OP_LMHEAD;
-      P.ss_in = h->at<float>(h->L.ss_x);
-      P.ss_parts = H / 128;
-      P.ss_stride = R;
-      P.logits = logits;
-      P.vocab = c.vocab;
-      P.n_out = c.vocab;
-      P.best_v = h->at<float>(h->L.best_v);
-      P.best_i = h->at<int>(h->L.best_i);
-      P.drafted = drafted;
-      return run_gemv(h, P, nb, st);
-    }));
-  }
   return DFLASH_OK;
 }
 
@@ -638,6 +677,8 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   int chunks = std::max(1, std::min(kMaxChunks, ceil_div(2LL * h->n_sms, static_cast<long long>(batch) * block)));
   P.chunk_len = static_cast<int>(align_up(static_cast<size_t>(ceil_div(c.vocab, chunks)), 1024));
   P.chunks = ceil_div(c.vocab, P.chunk_len);
+  P.tl = tl_take(h, static_cast<long long>(P.chunks) * block * batch);
+  P.tl_id = h->tl_launch++;
   if (launch_verify(P, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
   note_launch(h, st);
   return DFLASH_OK;
@@ -689,6 +730,17 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear) {
 }
 
 int32_t dflash_last_launch_count(const dflash_handle* h) { return h ? h->last_launches : 0; }
+
+int dflash_timeline(dflash_handle* h, void* records, int64_t n_records) {
+  if (!h || n_records < 0 || (n_records > 0 && !records)) return DFLASH_E_INVAL;
+  h->tl_buf = n_records > 0 ? static_cast<unsigned long long*>(records) : nullptr;
+  h->tl_cap = n_records;
+  h->tl_next = 0;
+  h->tl_launch = 0;
+  return DFLASH_OK;
+}
+
+int64_t dflash_timeline_used(const dflash_handle* h) { return h ? h->tl_next : 0; }
 
 int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events) {
   if (!h || n_events < 0 || (n_events > 0 && !events)) return DFLASH_E_INVAL;

@@ -330,8 +330,44 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
   }
 }
 
+// Grid-wide phase barrier: every CTA arrives once per phase after its epilogue work is
+// done; a waiter sees all of that phase's stores. Bounded: false after kWaitLimitNs.
+DEV int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DEV bool grid_wait(const int* bar, int target) {
+  if (ld_acquire_gpu(bar) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(bar) >= target) return true;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+// Order this thread's generic-proxy global stores before later async-proxy (TMA) reads.
+DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Units of phase P are split over the first Gp = min(G, U) CTAs so that every participating
+// CTA has at least one unit (the split-tile bookkeeping counts consecutive participants);
+// CTAs c >= Gp have none in this phase but still take part in its barrier.
+DEV void phase_units(const GemvParams& P, int c, int G, uint32_t& U, uint32_t& u0, uint32_t& u1, int& Gp) {
+  U = static_cast<uint32_t>(P.T) * P.KB;
+  Gp = static_cast<uint32_t>(G) < U ? G : static_cast<int>(U);
+  if (c < Gp) {
+    u0 = unit_begin(c, U, Gp);
+    u1 = unit_begin(c + 1, U, Gp);
+  } else {
+    u0 = u1 = U;
+  }
+}
+
+// A chain of projection phases in one persistent launch. Phase p+1 reads what phase p
+// wrote, so its activation tiles are loaded only after the phase-p grid barrier, but its
+// weight tiles are streamed into every free ring stage before that barrier.
 template <class C>
-__global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constant__ GemvParams P) {
+__global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constant__ GemvChain CH) {
   constexpr int NB = C::ROWS / 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -346,12 +382,18 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
-  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);  // [0] last-arrival flag, [1..2] wait ok by tile parity
+  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);  // [0] last arrival, [1..2] wait ok by tile parity, [3] phase ok
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
-  const uint32_t U = static_cast<uint32_t>(P.T) * P.KB;
-  const uint32_t u0 = unit_begin(c, U, G), u1 = unit_begin(c + 1, U, G);
+  const int NP = CH.n_phases;
+  int* err = CH.ph[0].err;
+  unsigned long long* tl = CH.tl ? CH.tl + static_cast<size_t>(c) * kTlWords : nullptr;
+  if (tl && threadIdx.x == 0) {
+    tl[0] = (static_cast<unsigned long long>(TL_GEMV) << 32) | static_cast<unsigned>(CH.tl_id);
+    tl[1] = smid();
+    tl_stamp(tl, 2);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -365,8 +407,10 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < P.n_amaps; ++i) tma_prefetch_desc(&P.amap[i]);
-    tma_prefetch_desc(&P.bmap);
+    for (int p = 0; p < NP; ++p) {
+      for (int i = 0; i < CH.ph[p].n_amaps; ++i) tma_prefetch_desc(&CH.ph[p].amap[i]);
+      tma_prefetch_desc(&CH.ph[p].bmap);
+    }
   }
   if (warp == 1) {
     tmem_alloc(s_tmem, C::TMEM_COLS);
@@ -376,6 +420,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  if (threadIdx.x == 0) tl_stamp(tl, 3);
   // Every thread but the producer waits for the previous kernel now and then lets the next
   // one start; the producer first streams weights that do not depend on it.
   if (!(warp == 0 && lane == 0)) {
@@ -388,39 +433,68 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       // ------------------------------------------------ TMA producer
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint32_t n = u1 - u0;
-      const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
-      for (uint32_t i = 0; i < pre; ++i) {  // weights do not depend on the previous kernel
-        const uint32_t u = u0 + i;
-        mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-        load_a<C::KS>(P, u / P.KB, u % P.KB, sA + i * C::A_BYTES, &full[i], pol_w);
-      }
-      pdl_wait();
-      // The grid this kernel depends on has completed, so everything it (or anything before
-      // it) wrote is visible: from here on the next kernel may start and prefetch.
-      pdl_launch_dependents();
-      for (uint32_t i = 0; i < pre; ++i) {
-        const uint32_t u = u0 + i;
-        load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + i * C::B_BYTES, &full[i], pol_x);
-      }
-      uint32_t issued = pre;
-      for (uint32_t i = pre; i < n; ++i) {
-        const uint32_t s = i % C::STAGES, r = i / C::STAGES;
-        if (!mbar_wait(&empty[s], (r - 1) & 1)) {
-          raise_flag(P.err, kDevTimeout);
+      uint32_t it = 0;  // stages armed with both weight and activation copies, over all phases
+      bool ok = true;
+      for (int p = 0; p < NP && ok; ++p) {
+        const GemvParams& P = CH.ph[p];
+        uint32_t U, u0, u1;
+        int Gp;
+        phase_units(P, c, G, U, u0, u1, Gp);
+        const uint32_t n = u1 > u0 ? u1 - u0 : 0;
+        const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
+        tl_stamp(tl, 4 + 4 * p);
+        uint32_t a_only = 0;  // weights do not depend on earlier phases: stream them first
+        for (; a_only < pre; ++a_only) {
+          const uint32_t i = it + a_only, s = i % C::STAGES, r = i / C::STAGES;
+          if (i >= static_cast<uint32_t>(C::STAGES) && !mbar_wait(&empty[s], (r - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t u = u0 + a_only;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
+        }
+        bool dep_ok = ok;
+        if (dep_ok) {
+          if (p == 0) {
+            pdl_wait();
+            pdl_launch_dependents();
+          } else {
+            dep_ok = grid_wait(CH.bar + p - 1, G);
+          }
+        }
+        tl_stamp(tl, 5 + 4 * p);
+        fence_proxy_async_global();
+        // activations of the stages armed above (issued even after a failed wait so that
+        // every armed stage completes and the drain below cannot stall)
+        for (uint32_t k = 0; k < a_only; ++k) {
+          const uint32_t u = u0 + k, s = (it + k) % C::STAGES;
+          load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+        }
+        it += a_only;
+        if (!ok || !dep_ok) {
+          ok = false;
           break;
         }
-        const uint32_t u = u0 + i;
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
-        load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
-        ++issued;
+        for (uint32_t k = pre; k < n; ++k) {
+          const uint32_t s = it % C::STAGES, r = it / C::STAGES;
+          if (!mbar_wait(&empty[s], (r - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t u = u0 + k;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
+          load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+          ++it;
+        }
       }
+      if (!ok) raise_flag(err, kDevTimeout);
       // drain: every copy this thread issued has landed before the CTA may exit
-      const uint32_t first = issued > static_cast<uint32_t>(C::STAGES) ? issued - C::STAGES : 0;
-      for (uint32_t i = first; i < issued; ++i)
+      const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0;
+      for (uint32_t i = first; i < it; ++i)
         if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1)) {
-          raise_flag(P.err, kDevTimeout);
+          raise_flag(err, kDevTimeout);
           break;
         }
     }
@@ -430,193 +504,230 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       uint32_t i = 0;
       int lt = 0;
       bool ok = true;
-      for (int t = static_cast<int>(u0 / P.KB); ok && static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
-        const uint32_t ub = max(u0, static_cast<uint32_t>(t) * P.KB);
-        const uint32_t ue = min(u1, static_cast<uint32_t>(t + 1) * P.KB);
-        const int acc = lt & 1;
-        if (lt >= 2 && !mbar_wait(&tempty[acc], ((lt >> 1) - 1) & 1)) {
-          raise_flag(P.err, kDevTimeout);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * C::ROWS;
-        for (uint32_t u = ub; u < ue; ++u, ++i) {
-          const uint32_t s = i % C::STAGES, r = i / C::STAGES;
-          if (!mbar_wait(&full[s], r & 1)) {
-            raise_flag(P.err, kDevTimeout);
+      for (int p = 0; p < NP && ok; ++p) {
+        const GemvParams& P = CH.ph[p];
+        uint32_t U, u0, u1;
+        int Gp;
+        phase_units(P, c, G, U, u0, u1, Gp);
+        if (u0 >= u1) continue;
+        for (int t = static_cast<int>(u0 / P.KB); ok && static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+          const uint32_t ub = max(u0, static_cast<uint32_t>(t) * P.KB);
+          const uint32_t ue = min(u1, static_cast<uint32_t>(t + 1) * P.KB);
+          const int acc = lt & 1;
+          if (lt >= 2 && !mbar_wait(&tempty[acc], ((lt >> 1) - 1) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
+          const uint32_t d_tmem = tmem + acc * C::ROWS;
+          for (uint32_t u = ub; u < ue; ++u, ++i) {
+            const uint32_t s = i % C::STAGES, r = i / C::STAGES;
+            if (!mbar_wait(&full[s], r & 1)) {
+              ok = false;
+              break;
+            }
+            if (u == u0) tl_stamp(tl, 6 + 4 * p);
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
-          for (int j = 0; j < C::KS; ++j)
+            for (int j = 0; j < C::KS; ++j)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32),
-                          smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), C::IDESC,
-                          (u > ub || j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&empty[s]);
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32),
+                            smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), C::IDESC,
+                            (u > ub || j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&empty[s]);
+          }
+          if (ok) tc_commit(&tfull[acc]);
         }
-        if (ok) tc_commit(&tfull[acc]);
       }
+      if (!ok) raise_flag(err, kDevTimeout);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int e = threadIdx.x - 64;
     const int q = warp & 3;
     const int m = q * 32 + lane;
-    pdl_wait();
-    if (P.ss_in) {
-      // inv_rms of every row of the pass: 8 lanes per row each sum a strided subset of the
-      // per-tile partials (all loads in flight at once), then a fixed lane tree combines them.
-      for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
-        const int r = r0 + (e >> 3), lane8 = e & 7;
-        const float* src = P.ss_in + P.ss_row0 + r;
-        float part = 0.f;
-#pragma unroll 4
-        for (int p = lane8; p < P.ss_parts; p += 8) part += __ldcg(src + static_cast<size_t>(p) * P.ss_stride);
-        part += __shfl_down_sync(0xffffffffu, part, 4, 8);
-        part += __shfl_down_sync(0xffffffffu, part, 2, 8);
-        part += __shfl_down_sync(0xffffffffu, part, 1, 8);
-        if (lane8 == 0) s_inv[r] = rsqrtf(part / static_cast<float>(P.H) + P.eps);
-      }
-    }
-    for (int r = e; r < C::ROWS; r += 128) {
-      s_bv[r] = -INFINITY;
-      s_bi[r] = 0x7fffffff;
-    }
-    named_bar_sync(1, 128);
     int lt = 0;
-    for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
-      const int acc = lt & 1;
-      float xpre[16];
-      if (NB == 1 && P.op == OP_RESID) {   // the residual this tile will update, read ahead
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          xpre[j] = (P.grow0 + j < P.n_valid) ? __ldcg(P.y + static_cast<size_t>(P.grow0 + j) * P.y_ld + t * 128 + m)
-                                               : 0.f;
+    bool alive = true;
+    for (int p = 0; p < NP && alive; ++p) {
+      const GemvParams& P = CH.ph[p];
+      uint32_t U, u0, u1;
+      int Gp;
+      phase_units(P, c, G, U, u0, u1, Gp);
+      if (p > 0) {
+        if (e == 0) s_misc[3] = grid_wait(CH.bar + p - 1, G) ? 1 : 0;
+        named_bar_sync(1, 128);
+        if (!s_misc[3]) {
+          if (e == 0) raise_flag(err, kDevTimeout);
+          alive = false;
+          break;
+        }
       }
-      if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
+      if (P.ss_in) {
+        // inv_rms of every row of the pass: 8 lanes per row each sum a strided subset of the
+        // per-tile partials (all loads in flight at once), then a fixed lane tree combines them.
+        for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
+          const int r = r0 + (e >> 3), lane8 = e & 7;
+          const float* src = P.ss_in + P.ss_row0 + r;
+          float part = 0.f;
+#pragma unroll 4
+          for (int pp = lane8; pp < P.ss_parts; pp += 8) part += __ldcg(src + static_cast<size_t>(pp) * P.ss_stride);
+          part += __shfl_down_sync(0xffffffffu, part, 4, 8);
+          part += __shfl_down_sync(0xffffffffu, part, 2, 8);
+          part += __shfl_down_sync(0xffffffffu, part, 1, 8);
+          if (lane8 == 0) s_inv[r] = rsqrtf(part / static_cast<float>(P.H) + P.eps);
+        }
+      }
+      for (int r = e; r < C::ROWS; r += 128) {
+        s_bv[r] = -INFINITY;
+        s_bi[r] = 0x7fffffff;
+      }
       named_bar_sync(1, 128);
-      if (!s_misc[1 + acc]) {
-        if (e == 0) raise_flag(P.err, kDevTimeout);
-        break;
-      }
-      tc_fence_after();
-      const int ca = cta_of_unit(static_cast<uint32_t>(t) * P.KB, U, G);
-      const int cb = cta_of_unit(static_cast<uint32_t>(t + 1) * P.KB - 1, U, G);
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ROWS;
-      if (ca == cb) {
-        for (int ch = 0; ch < NB; ++ch) {
-          float v[16];
-          tmem_ld16(taddr + ch * 16, v);
-          if (ch == NB - 1) {
+      if (u0 < u1) {
+        for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+          const int acc = lt & 1;
+          float xpre[16];
+          if (NB == 1 && P.op == OP_RESID) {   // the residual this tile will update, read ahead
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              xpre[j] = (P.grow0 + j < P.n_valid)
+                            ? __ldcg(P.y + static_cast<size_t>(P.grow0 + j) * P.y_ld + t * 128 + m)
+                            : 0.f;
+          }
+          if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
+          named_bar_sync(1, 128);
+          if (!s_misc[1 + acc]) {
+            if (e == 0) raise_flag(err, kDevTimeout);
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const int ca = cta_of_unit(static_cast<uint32_t>(t) * P.KB, U, Gp);
+          const int cb = cta_of_unit(static_cast<uint32_t>(t + 1) * P.KB - 1, U, Gp);
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ROWS;
+          if (ca == cb) {
+            for (int ch = 0; ch < NB; ++ch) {
+              float v[16];
+              tmem_ld16(taddr + ch * 16, v);
+              if (ch == NB - 1) {
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+              }
+              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
+            }
+          } else {
+            const int slot = part_slot(c, t, U, Gp, P.KB);
+            float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
+            for (int ch = 0; ch < NB; ++ch) {
+              float v[16];
+              tmem_ld16(taddr + ch * 16, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) dst[(ch * 16 + j) * 128 + m] = v[j];
+            }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
-          }
-          epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
-        }
-      } else {
-        const int slot = part_slot(c, t, U, G, P.KB);
-        float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
-        for (int ch = 0; ch < NB; ++ch) {
-          float v[16];
-          tmem_ld16(taddr + ch * 16, v);
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (e == 0) {
+              const int old = atomicAdd(P.tile_cnt + t, 1);
+              const int last = (old == cb - ca);
+              if (last) P.tile_cnt[t] = 0;
+              s_misc[0] = last;
+            }
+            named_bar_sync(1, 128);
+            if (s_misc[0]) {
+              __threadfence();
+              for (int ch = 0; ch < NB; ++ch) {
+                float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(ch * 16 + j) * 128 + m] = v[j];
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                for (int cc = ca; cc <= cb; cc += 2) {   // two segments' loads in flight per round
+                  const float* s0 = P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128;
+                  float a[16], b[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) a[j] = __ldcg(s0 + (ch * 16 + j) * 128 + m);
+                  if (cc + 1 <= cb) {
+                    const float* s1 =
+                        P.part + static_cast<size_t>(part_slot(cc + 1, t, U, Gp, P.KB)) * C::ROWS * 128;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) b[j] = __ldcg(s1 + (ch * 16 + j) * 128 + m);
+                  }
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[j] += a[j];
+                  if (cc + 1 <= cb) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += b[j];
+                  }
+                }
+                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
+              }
+            }
+          }
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+      }
+      if (!alive) break;
+
+      // ---------------------------------------------- phase-level completion hooks
+      if (P.op == OP_LMHEAD || (P.op == OP_KV && P.commit_len)) {
+        named_bar_sync(1, 128);
+        if (P.op == OP_LMHEAD) {
+          for (int r = e; r < C::ROWS; r += 128) {
+            P.best_v[c * kMaxPassRows + r] = s_bv[r];
+            P.best_i[c * kMaxPassRows + r] = s_bi[r];
+          }
+        }
         __threadfence();
         named_bar_sync(1, 128);
         if (e == 0) {
-          const int old = atomicAdd(P.tile_cnt + t, 1);
-          const int last = (old == cb - ca);
-          if (last) P.tile_cnt[t] = 0;
+          const int old = atomicAdd(P.cta_cnt, 1);
+          const int last = (old == G - 1);
+          if (last) *P.cta_cnt = 0;
           s_misc[0] = last;
         }
         named_bar_sync(1, 128);
         if (s_misc[0]) {
           __threadfence();
-          for (int ch = 0; ch < NB; ++ch) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            for (int cc = ca; cc <= cb; cc += 2) {   // two segments' loads in flight per round
-              const float* s0 = P.part + static_cast<size_t>(part_slot(cc, t, U, G, P.KB)) * C::ROWS * 128;
-              float a[16], b[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) a[j] = __ldcg(s0 + (ch * 16 + j) * 128 + m);
-              if (cc + 1 <= cb) {
-                const float* s1 = P.part + static_cast<size_t>(part_slot(cc + 1, t, U, G, P.KB)) * C::ROWS * 128;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) b[j] = __ldcg(s1 + (ch * 16 + j) * 128 + m);
+          if (P.op == OP_LMHEAD) {
+            const int B = P.rows_per_seq;
+            for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
+              const int r = r0 + (e >> 3), lane8 = e & 7;
+              float bv = -INFINITY;
+              int bi = 0x7fffffff;
+#pragma unroll 4
+              for (int cc = lane8; cc < G; cc += 8) {
+                const float ov = __ldcg(P.best_v + cc * kMaxPassRows + r);
+                const int oi = __ldcg(P.best_i + cc * kMaxPassRows + r);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
               }
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += a[j];
-              if (cc + 1 <= cb) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] += b[j];
+              for (int off = 4; off >= 1; off >>= 1) {
+                const float ov = __shfl_down_sync(0xffffffffu, bv, off, 8);
+                const int oi = __shfl_down_sync(0xffffffffu, bi, off, 8);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+              }
+              const int gr = P.grow0 + r;
+              if (lane8 == 0 && gr < P.n_valid) {
+                const int s = gr / B, i = gr - s * B;
+                if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
               }
             }
-            epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
+          } else {
+            for (int s = e; s < P.batch; s += 128) {
+              const int nl = __ldcg(P.len + s) + __ldcg(P.n_new + s);
+              P.len[s] = nl < P.cap ? nl : P.cap;
+            }
           }
         }
       }
-    }
-
-    // ------------------------------------------------ CTA-level completion hooks
-    if (P.op == OP_LMHEAD || (P.op == OP_KV && P.commit_len)) {
-      named_bar_sync(1, 128);
-      if (P.op == OP_LMHEAD) {
-        for (int r = e; r < C::ROWS; r += 128) {
-          P.best_v[c * kMaxPassRows + r] = s_bv[r];
-          P.best_i[c * kMaxPassRows + r] = s_bi[r];
-        }
-      }
+      // ---------------------------------------------- arrive at this phase's barrier
+      fence_proxy_async_global();
       __threadfence();
       named_bar_sync(1, 128);
       if (e == 0) {
-        const int old = atomicAdd(P.cta_cnt, 1);
-        const int last = (old == G - 1);
-        if (last) *P.cta_cnt = 0;
-        s_misc[0] = last;
-      }
-      named_bar_sync(1, 128);
-      if (s_misc[0]) {
-        __threadfence();
-        if (P.op == OP_LMHEAD) {
-          const int B = P.rows_per_seq;
-          for (int r0 = 0; r0 < C::ROWS; r0 += 16) {
-            const int r = r0 + (e >> 3), lane8 = e & 7;
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll 4
-            for (int cc = lane8; cc < G; cc += 8) {
-              const float ov = __ldcg(P.best_v + cc * kMaxPassRows + r);
-              const int oi = __ldcg(P.best_i + cc * kMaxPassRows + r);
-              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-#pragma unroll
-            for (int off = 4; off >= 1; off >>= 1) {
-              const float ov = __shfl_down_sync(0xffffffffu, bv, off, 8);
-              const int oi = __shfl_down_sync(0xffffffffu, bi, off, 8);
-              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            const int gr = P.grow0 + r;
-            if (lane8 == 0 && gr < P.n_valid) {
-              const int s = gr / B, i = gr - s * B;
-              if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
-            }
-          }
-        } else {
-          for (int s = e; s < P.batch; s += 128) {
-            const int nl = __ldcg(P.len + s) + __ldcg(P.n_new + s);
-            P.len[s] = nl < P.cap ? nl : P.cap;
-          }
-        }
+        tl_stamp(tl, 7 + 4 * p);
+        atomicAdd(CH.bar + p, 1);
       }
     }
   }
@@ -625,10 +736,19 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (threadIdx.x == 0) {  // the last CTA out clears the barrier counters for the next launch
+    tl_stamp(tl, 20);
+    __threadfence();
+    if (atomicAdd(CH.exit_cnt, 1) == G - 1) {
+      for (int p = 0; p < NP; ++p) CH.bar[p] = 0;
+      *CH.exit_cnt = 0;
+      __threadfence();
+    }
+  }
 }
 
 template <class C>
-static int launch_cfg(const GemvParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
+static int launch_cfg(const GemvChain& p, int n_ctas, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(192);
@@ -680,7 +800,7 @@ int gemv_set_attributes() {
   return e;
 }
 
-int launch_gemv(const GemvParams& p, int variant, int n_ctas, cudaStream_t stream, bool pdl) {
+int launch_gemv(const GemvChain& p, int variant, int n_ctas, cudaStream_t stream, bool pdl) {
 #define DFL_LAUNCH(ID, NB, KS, ST, MB) \
   if (variant == ID) return launch_cfg<GemvCfg<NB, KS, ST, MB>>(p, n_ctas, stream, pdl);
   DFL_GEMV_VARIANTS(DFL_LAUNCH)

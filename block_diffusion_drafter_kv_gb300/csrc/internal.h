@@ -84,11 +84,32 @@ struct GemvParams {
   int* drafted;
 };
 
+// Up to kMaxPhases projections run back to back in one persistent launch: phase p+1 may
+// read what phase p wrote (grid barrier in between); weights of phase p+1 are streamed
+// before the barrier. Every CTA must be resident at once (grid <= SMs, one CTA per SM).
+constexpr int kMaxPhases = 4;
+struct GemvChain {
+  GemvParams ph[kMaxPhases];
+  int n_phases;
+  int* bar;       // [kMaxPhases] arrival counters, zero at launch; cleared by the last CTA out
+  int* exit_cnt;  // [1]
+  unsigned long long* tl;  // per-CTA timeline records (kTlWords each) or null
+  int tl_id;               // launch id written into the records
+};
+
+// Timeline record of one CTA (kTlWords 64-bit words, %globaltimer nanoseconds):
+//   [0] (kind << 32) | launch id   [1] SM id   [2] entry   [3] set-up done
+//   [4 + 4p] phase p: producer starts it   [5 + 4p] its input is ready (previous phase / kernel)
+//   [6 + 4p] first operand stage landed    [7 + 4p] epilogue done with it
+//   [20] exit
+constexpr int kTlWords = 21;
+enum TlKind : int { TL_GEMV = 1, TL_ATTN = 2, TL_EMBED = 3, TL_VERIFY = 4 };
+
 // Kernel variant for nb activation row groups of 16 (1, 2, 4, 8 or 16); `pref` selects
 // among the nb == 1 variants. KB of a launch counts k-stages of 64 * gemv_variant_ksub(v).
 int gemv_variant(int nb, int pref);
 int gemv_variant_ksub(int variant);
-int launch_gemv(const GemvParams& p, int variant, int n_ctas, cudaStream_t stream, bool pdl);
+int launch_gemv(const GemvChain& p, int variant, int n_ctas, cudaStream_t stream, bool pdl);
 int gemv_set_attributes();
 
 // ---------------------------------------------------------------- block attention
@@ -101,6 +122,8 @@ struct AttnParams {
   int* err;
   int B, nq, nkv, d, cap;
   float scale_log2;        // log2(e) / sqrt(d)
+  unsigned long long* tl;  // timeline records (kTlWords per CTA) or null
+  int tl_id;
 };
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
 int attn_set_attributes();
@@ -118,6 +141,8 @@ struct EmbedParams {
   float* trace;                   // [rows][H] or null
   int* err;
   int B, H, V, cap;
+  unsigned long long* tl;
+  int tl_id;
 };
 int launch_embed(const EmbedParams& p, int batch, cudaStream_t stream, bool pdl);
 
@@ -132,6 +157,8 @@ struct VerifyParams {
   int* seq_cnt;         // [batch]
   int* err;
   int B, V, chunks, chunk_len;
+  unsigned long long* tl;
+  int tl_id;
 };
 int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pdl);
 

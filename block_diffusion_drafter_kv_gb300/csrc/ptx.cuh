@@ -190,6 +190,16 @@ DEV float ld_shared_cluster_f32(uint32_t addr) {
   return v;
 }
 
+// ---------------------------------------------------------------- timeline stamps
+DEV unsigned smid() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %smid;" : "=r"(r));
+  return r;
+}
+DEV void tl_stamp(unsigned long long* rec, int slot) {
+  if (rec) rec[slot] = globaltimer_ns();
+}
+
 // ---------------------------------------------------------------- misc
 DEV float ld_cg_f32(const float* p) { return __ldcg(p); }
 

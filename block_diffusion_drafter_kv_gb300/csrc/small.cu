@@ -12,8 +12,15 @@ namespace dfl {
 // All loads of a thread are issued before any of its stores (the buffers could alias as far
 // as the compiler knows), so the kernel costs one memory round trip, not one per element.
 __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
+  unsigned long long* tl = P.tl ? P.tl + static_cast<size_t>(blockIdx.x) * kTlWords : nullptr;
+  if (tl && threadIdx.x == 0) {
+    tl[0] = (static_cast<unsigned long long>(TL_EMBED) << 32) | static_cast<unsigned>(P.tl_id);
+    tl[1] = smid();
+    tl_stamp(tl, 2);
+  }
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0) tl_stamp(tl, 5);
   constexpr int kMaxIter = 4;  // H <= 4 * 8 * blockDim
   const int row = blockIdx.x;
   const int s = row / P.B, i = row - s * P.B;
@@ -60,6 +67,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
       *reinterpret_cast<float4*>(P.trace + off + 4) = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
+  if (threadIdx.x == 0) tl_stamp(tl, 20);
   __shared__ float red[8];
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
@@ -99,8 +107,15 @@ DEV void better(float& bv, int& bi, float ov, int oi) {
 }
 
 __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
+  unsigned long long* tl = P.tl ? P.tl + static_cast<size_t>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kTlWords : nullptr;
+  if (tl && threadIdx.x == 0) {
+    tl[0] = (static_cast<unsigned long long>(TL_VERIFY) << 32) | static_cast<unsigned>(P.tl_id);
+    tl[1] = smid();
+    tl_stamp(tl, 2);
+  }
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0) tl_stamp(tl, 5);
   const int chunk = blockIdx.x, i = blockIdx.y, s = blockIdx.z;
   const int B = P.B, V = P.V;
   const float* row = P.logits + (static_cast<size_t>(s) * B + i) * V;
@@ -137,6 +152,7 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
     const int oi = __shfl_down_sync(0xffffffffu, bi, o);
     better(bv, bi, ov, oi);
   }
+  if (threadIdx.x == 0) tl_stamp(tl, 20);
   __shared__ float wv[8];
   __shared__ int wi[8];
   __shared__ int s_last;
