@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
       *s_abort = 1;
       raise_flag(P.err, kDevTimeout);
     }
+    if (i == 0 && threadIdx.x == 0) tl_stamp(tl, 6);
     const uint32_t kb = smem_u32(smem + st * 2 * TILE_BYTES);
     const uint32_t vb = kb + TILE_BYTES;
     const int key0 = (t0 + i) * KT;
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     }
   }
 
+  if (threadIdx.x == 0) tl_stamp(tl, 7);
   // row sums across the quad
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -285,36 +287,65 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   }
   cluster_sync();
 
-  // merge: this CTA owns rows [rb0, rb1) of the nw*16 query rows
+  if (threadIdx.x == 0) tl_stamp(tl, 8);
+  // merge: this CTA owns rows [rb0, rb1) of the nw*16 query rows. First every (row, split)
+  // pair's max and sum are fetched in parallel, then each row's split weights are formed.
   const int R = nw * 16;
   const int per = (R + S - 1) / S;
   const int rb0 = rank * per, rb1 = min(R, rb0 + per);
-  for (int rr = rb0 + static_cast<int>(threadIdx.x); rr < rb1; rr += blockDim.x) {
-    float M = -INFINITY;
-    for (int c = 0; c < S; ++c) M = fmaxf(M, ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c)));
-    float den = 0.f;
-    for (int c = 0; c < S; ++c) {
-      const float mc = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c));
-      const float lc = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_l[rr]), c));
-      const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
-      s_w[(rr - rb0) * 16 + c] = w;
-      den += w * lc;
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int c = 0; c < S; ++c) s_w[(rr - rb0) * 16 + c] *= inv;
+  const int nrow = max(rb1 - rb0, 0);
+  float* s_wm = s_w;              // [rows][S] remote maxima, then weights (rows*S <= 144)
+  float* s_wl = s_w + 1024;       // [rows][S] remote sums
+  for (int k = threadIdx.x; k < nrow * S; k += blockDim.x) {
+    const int rr = rb0 + k / S, c = k % S;
+    s_wm[(rr - rb0) * S + c] = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c));
+    s_wl[(rr - rb0) * S + c] = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_l[rr]), c));
   }
   __syncthreads();
-  const int cnt = (rb1 - rb0) * D;
-  for (int idx = threadIdx.x; idx < cnt; idx += blockDim.x) {
-    const int rr = rb0 + idx / D, d = idx % D;
+  for (int k = threadIdx.x; k < nrow; k += blockDim.x) {
+    float M = -INFINITY;
+    for (int c = 0; c < S; ++c) M = fmaxf(M, s_wm[k * S + c]);
+    float den = 0.f;
+    for (int c = 0; c < S; ++c) {
+      const float mc = s_wm[k * S + c];
+      const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
+      s_wm[k * S + c] = w;
+      den += w * s_wl[k * S + c];
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = 0; c < S; ++c) s_wm[k * S + c] *= inv;
+  }
+  __syncthreads();
+  // combine: a thread takes 4 consecutive d of one row and reads all splits' values at once
+  constexpr int kMaxSplit = 16;
+  const int items = nrow * (D / 4);
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int rr = rb0 + it / (D / 4), d = (it % (D / 4)) * 4;
     const int w = rr >> 4, slot = rr & 15;
     if (slot >= B) continue;
-    float acc = 0.f;
-    for (int c = 0; c < S; ++c)
-      acc += s_w[(rr - rb0) * 16 + c] * ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_o[rr * D + d]), c));
-    P.o[(static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d] =
-        __float2bfloat16_rn(acc);
+    float4 part[kMaxSplit];
+    const uint32_t a = smem_u32(&s_o[rr * D + d]);
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c)
+      if (c < S) part[c] = ld_shared_cluster_v4(map_shared_rank(a, c));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c)
+      if (c < S) {
+        const float wt = s_wm[(rr - rb0) * S + c];
+        acc.x += wt * part[c].x;
+        acc.y += wt * part[c].y;
+        acc.z += wt * part[c].z;
+        acc.w += wt * part[c].w;
+      }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(P.o + (static_cast<size_t>(seq) * B + slot) * nq * D +
+                              static_cast<size_t>(g * nw + w) * D + d) = pk;
   }
+  if (threadIdx.x == 0) tl_stamp(tl, 9);
   if (threadIdx.x == 0) tl_stamp(tl, 20);
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }

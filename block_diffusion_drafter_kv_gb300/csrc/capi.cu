@@ -149,6 +149,7 @@ struct dflash_handle {
   int inject_pass_rows = 16;
   int gemv_pref = 2;  // weight-streaming kernel variant for single-row-group launches
   int chain_slot = 0;
+  int chain_max = kMaxPhases;  // projections per persistent launch (1 = one launch per projection)
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -207,7 +208,20 @@ void note_launch(dflash_handle* h, cudaStream_t st) {
 
 // One persistent launch over a chain of projection phases (all with nb row groups). Each
 // phase's KB arrives in 64-wide k-blocks; the kernel variant may stage several per step.
+#define DFL_TRY(x)                \
+  do {                            \
+    const int _r = (x);           \
+    if (_r != DFLASH_OK) return _r; \
+  } while (0)
+
+int run_chain_one(dflash_handle* h, const GemvParams* phases, int n, int nb, cudaStream_t st);
+
 int run_chain(dflash_handle* h, const GemvParams* phases, int n, int nb, cudaStream_t st) {
+  for (int p0 = 0; p0 < n; p0 += h->chain_max) DFL_TRY(run_chain_one(h, phases + p0, std::min(h->chain_max, n - p0), nb, st));
+  return DFLASH_OK;
+}
+
+int run_chain_one(dflash_handle* h, const GemvParams* phases, int n, int nb, cudaStream_t st) {
   GemvChain C{};
   int v = gemv_variant(nb, h->gemv_pref);
   int ks = gemv_variant_ksub(v);
@@ -235,11 +249,6 @@ int run_chain(dflash_handle* h, const GemvParams* phases, int n, int nb, cudaStr
 
 int run_gemv(dflash_handle* h, const GemvParams& P, int nb, cudaStream_t st) { return run_chain(h, &P, 1, nb, st); }
 
-#define DFL_TRY(x)                \
-  do {                            \
-    const int _r = (x);           \
-    if (_r != DFLASH_OK) return _r; \
-  } while (0)
 
 }  // namespace
 
@@ -285,6 +294,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
   if (const char* ev = std::getenv("DFLASH_GEMV_VARIANT")) h->gemv_pref = std::atoi(ev);
+  if (const char* ev = std::getenv("DFLASH_CHAIN_MAX")) h->chain_max = std::max(1, std::min(kMaxPhases, std::atoi(ev)));
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
       gemv_set_attributes() != 0 || attn_set_attributes() != 0) {

@@ -41,7 +41,7 @@ struct GemvCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * ROWS < 32 ? 32 : 2 * ROWS;
   static constexpr int XLD = 132;                     // padded row of the exchange buffer
-  static constexpr int EPI_BYTES = 16 * XLD * 4 + 3 * ROWS * 4;
+  static constexpr int EPI_BYTES = 16 * XLD * 4 + 5 * ROWS * 4;  // xch, inv, best v/i, row pos/seq
   static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(128, ROWS);
@@ -128,22 +128,27 @@ DEV void rope16(float (&val)[16], const int (&pos)[16], int m, int d, const floa
   const int jh = m & (d - 1);
   const int fi = jh & (half - 1);
   const bool lo = jh < half;
+  float cs[16], sn[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {  // table reads in flight while the exchange completes
+    cs[j] = __ldg(cosT + pos[j] * half + fi);
+    sn[j] = __ldg(sinT + pos[j] * half + fi);
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) xch[j * XLD + m] = val[j];
   named_bar_sync(1, 128);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float p = xch[j * XLD + (m ^ half)];
-    const float c = cosT[pos[j] * half + fi];
-    const float s = sinT[pos[j] * half + fi];
-    val[j] = lo ? (val[j] * c - p * s) : (val[j] * c + p * s);
+    val[j] = lo ? (val[j] * cs[j] - p * sn[j]) : (val[j] * cs[j] + p * sn[j]);
   }
   named_bar_sync(1, 128);
 }
 
 template <int NB, int XLD>
 DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], int m, int e, float* xch,
-                        const float* s_inv, float* s_bv, int* s_bi, const float (&xpre)[16]) {
+                        const float* s_inv, float* s_bv, int* s_bi, const float (&xpre)[16], const int* s_pos,
+                        const int* s_seq) {
   const int lr0 = chunk * 16;          // local row of v[0]
   const int gr0 = P.grow0 + lr0;       // global row of v[0]
   switch (P.op) {
@@ -172,37 +177,19 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
       const int feat = (t - P.tile_start[mi]) * 128 + m;  // head*d + j within Wk / Wv
       float val[16];
       int pos[16];
-      bool ok[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         val[j] = v[j] * s_inv[lr0 + j];
-        const int gr = gr0 + j;
-        const int s = gr / P.rows_per_seq, r = gr - s * P.rows_per_seq;
-        int p = 0;
-        bool valid = false;
-        if (s < P.batch) {
-          const int nn = __ldcg(P.n_new + s);
-          if (r < nn) {
-            p = __ldcg(P.len + s) + r;
-            valid = true;
-            if (p >= P.cap) {
-              valid = false;
-              if (feat == 0) raise_flag(P.err, kDevCapacity);
-            }
-          }
-        }
-        ok[j] = valid;
-        pos[j] = valid ? p : 0;
+        pos[j] = max(s_pos[lr0 + j], 0);   // row positions were resolved once per phase
       }
       if (!is_v) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
       __nv_bfloat16* cache = is_v ? P.vc : P.kc;
       const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        if (!ok[j]) continue;
-        const int gr = gr0 + j;
-        const int s = gr / P.rows_per_seq;
-        const size_t off = ((static_cast<size_t>(layer) * P.max_batch + s) * P.cap + pos[j]) * row_elems + feat;
+        if (s_pos[lr0 + j] < 0) continue;
+        const size_t off =
+            ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
         cache[off] = f2bf(val[j]);
       }
     } break;
@@ -210,26 +197,12 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
     case OP_QKV: {
       const int mi = map_of_tile(P, t);  // 0 = q, 1 = k, 2 = v
       const int feat = (t - P.tile_start[mi]) * 128 + m;
-      const int B = P.rows_per_seq;
       float val[16];
       int pos[16];
-      bool ok[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         val[j] = v[j] * s_inv[lr0 + j];
-        const int gr = gr0 + j;
-        const int s = gr / B, i = gr - s * B;
-        int p = 0;
-        bool valid = gr < P.n_valid;
-        if (valid) {
-          p = __ldcg(P.len + s) + i;
-          if (p >= P.cap) {
-            valid = false;
-            if (feat == 0 && mi == 1) raise_flag(P.err, kDevCapacity);
-          }
-        }
-        ok[j] = valid;
-        pos[j] = valid ? p : 0;
+        pos[j] = max(s_pos[lr0 + j], 0);
       }
       if (mi < 2) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
       if (mi == 0) {
@@ -241,9 +214,9 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          if (!ok[j]) continue;
-          const int s = (gr0 + j) / B;
-          const size_t off = ((static_cast<size_t>(P.layer) * P.max_batch + s) * P.cap + pos[j]) * row_elems + feat;
+          if (s_pos[lr0 + j] < 0) continue;
+          const size_t off =
+              ((static_cast<size_t>(P.layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
           cache[off] = f2bf(val[j]);
         }
       }
@@ -377,7 +350,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   float* s_inv = xch + 16 * C::XLD;
   float* s_bv = s_inv + C::ROWS;
   int* s_bi = reinterpret_cast<int*>(s_bv + C::ROWS);
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_bi + C::ROWS);
+  int* s_pos = s_bi + C::ROWS;   // per row of the pass: cache position, or -1 if not written
+  int* s_seq = s_pos + C::ROWS;  // per row of the pass: sequence
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_seq + C::ROWS);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -583,6 +558,20 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       for (int r = e; r < C::ROWS; r += 128) {
         s_bv[r] = -INFINITY;
         s_bi[r] = 0x7fffffff;
+        if (P.op == OP_KV || P.op == OP_QKV) {  // where each row of the pass goes in the cache
+          const int gr = P.grow0 + r;
+          const int sq = gr / P.rows_per_seq, i = gr - sq * P.rows_per_seq;
+          int pos = -1;
+          if (P.op == OP_KV ? (sq < P.batch && i < __ldcg(P.n_new + sq)) : (gr < P.n_valid)) {
+            pos = __ldcg(P.len + sq) + i;
+            if (pos >= P.cap) {
+              raise_flag(P.err, kDevCapacity);
+              pos = -1;
+            }
+          }
+          s_pos[r] = pos;
+          s_seq[r] = sq;
+        }
       }
       named_bar_sync(1, 128);
       if (u0 < u1) {
@@ -615,7 +604,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
               }
-              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
+              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq);
             }
           } else {
             const int slot = part_slot(c, t, U, Gp, P.KB);
@@ -661,7 +650,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                     for (int j = 0; j < 16; ++j) v[j] += b[j];
                   }
                 }
-                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre);
+                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq);
               }
             }
           }
