@@ -90,22 +90,29 @@ def attn_bytes_flops(s, batch, B, n_ctx):
     return kvb + qo, fl
 
 
-def launch_plan(s, batch, B, tau, n_ctx):
+def launch_plan(s, batch, B, tau, n_ctx, n_sms=152):
     """Launch order of one step by call: (label, kind, bytes, flops). kind "gemv" marks the
-    weight-streaming kernel (one launch runs a chain of projections)."""
+    chained kernel (one launch runs up to DFLASH_CHAIN_MAX phases); attention is a launch of
+    its own between chains. Mirrors the library's grouping."""
     pj = proj_bytes_flops(s, batch, B, tau)
-    add = lambda *ks: tuple(map(sum, zip(*[pj[k] for k in ks])))
     ab = attn_bytes_flops(s, batch, B, n_ctx)
-    draft = [("embed", "small", 2 * s.hidden * batch * (1 + 6 * B), 0), ("qkv", "gemv", *pj["qkv"])]
+    chain_max = int(os.environ.get("DFLASH_CHAIN_MAX", "8"))
+    segments = [[("qkv", *pj["qkv"])]]
     for l in range(s.n_layers):
-        last = l == s.n_layers - 1
-        draft.append(("attn", "attn", *ab))
-        if last:
-            draft.append(("o+gateup+down+lm_head", "gemv", *add("o", "gateup", "down", "lm_head")))
-        else:
-            draft.append(("o+gateup+down+qkv", "gemv", *add("o", "gateup", "down", "qkv")))
+        tail = ("qkv", *pj["qkv"]) if l + 1 < s.n_layers else ("lm_head", *pj["lm_head"])
+        body = [("o", *pj["o"]), ("gateup", *pj["gateup"]), ("down", *pj["down"]), tail]
+        segments += ["attn", body]
+    draft = [("embed", "small", 2 * s.hidden * batch * (1 + 6 * B), 0)]
+    for seg in segments:
+        if seg == "attn":
+            draft.append(("attn", "attn", *ab))
+            continue
+        for i in range(0, len(seg), chain_max):
+            cur = seg[i:i + chain_max]
+            draft.append(("+".join(n for n, _, _ in cur), "gemv", sum(b for _, b, _ in cur),
+                          sum(f for _, _, f in cur)))
     return {
-        "inject": [("fc+kv", "gemv", *add("fc", "kv"))],
+        "inject": [("fc+kv", "gemv", *tuple(map(sum, zip(pj["fc"], pj["kv"]))))],
         "draft": draft,
         "verify": [("verify", "small", 4 * batch * B * s.vocab, 0)],
     }

@@ -13,6 +13,7 @@
 // memory by TMA. QKᵀ and PV run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
 // accumulate) with an online softmax in registers. The CTAs' partial (max, sum, output)
 // are merged through distributed shared memory in a fixed order, so no partials touch HBM.
+#include "attn_tile.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -20,37 +21,8 @@ namespace dfl {
 
 namespace {
 
-constexpr int KT = 64;       // keys per tile
+constexpr int KT = kAttnKeys;  // keys per tile
 constexpr int STAGES = 3;
-
-DEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-DEV void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-DEV uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Byte address of element (key, d) in a K or V tile: D/64 TMA boxes of 64 keys x 128 bytes,
-// each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
-DEV uint32_t kv_addr(uint32_t base, int key, int d) {
-  const int box = d >> 6, dd = d & 63;
-  return base + box * (KT * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
-}
 
 }  // namespace
 
@@ -139,27 +111,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   const int nq = P.nq;
   const int h = g * nw + warp;
   const int r0 = lane >> 2, kq = (lane & 3) * 2;
-  uint32_t qa[D / 16][4];
-  {
-    const size_t ld = static_cast<size_t>(nq) * D;
-    const __nv_bfloat16* qrow0 = P.q + (static_cast<size_t>(seq) * B + r0) * ld + h * D;
-    const __nv_bfloat16* qrow1 = qrow0 + 8 * ld;
-    const bool v0 = r0 < B, v1 = r0 + 8 < B;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int c = kk * 16 + kq;
-      qa[kk][0] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow0 + c)) : 0u;
-      qa[kk][1] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow1 + c)) : 0u;
-      qa[kk][2] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow0 + c + 8)) : 0u;
-      qa[kk][3] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(qrow1 + c + 8)) : 0u;
-    }
-  }
-
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float o[NT_D][4];
-#pragma unroll
-  for (int i = 0; i < NT_D; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  FaState<D> fa;
+  fa_begin<D>(fa, P.q, static_cast<size_t>(seq) * B, static_cast<size_t>(nq) * D, h, B, lane);
 
   for (int i = 0; i < n; ++i) {
     const int st = i % STAGES;
@@ -169,86 +122,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     }
     if (i == 0 && threadIdx.x == 0) tl_stamp(tl, 6);
     const uint32_t kb = smem_u32(smem + st * 2 * TILE_BYTES);
-    const uint32_t vb = kb + TILE_BYTES;
-    const int key0 = (t0 + i) * KT;
-
-    float sc[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int mi = lane >> 3;
-        const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
-        const int d = kk * 16 + (mi & 1) * 8;
-        uint32_t b[4];
-        ldsm_x4(kv_addr(kb, key, d), b);
-        mma_bf16_16816(sc[2 * np], qa[kk], b[0], b[1]);
-        mma_bf16_16816(sc[2 * np + 1], qa[kk], b[2], b[3]);
-      }
-    }
-    // scale to log2 units, mask keys past the end, online softmax
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int key = key0 + j * 8 + kq + (c & 1);
-        const float v = key < nkeys ? sc[j][c] * P.scale_log2 : -INFINITY;
-        sc[j][c] = v;
-        mx[c >> 1] = fmaxf(mx[c >> 1], v);
-      }
-    }
-    float corr[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mnew = fmaxf(m_run[r], mx[r]);
-      const float base = mnew == -INFINITY ? 0.f : mnew;
-      corr[r] = exp2f(m_run[r] - base);
-      m_run[r] = mnew;
-      mx[r] = base;
-    }
-    float ls[2] = {0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float p = exp2f(sc[j][c] - mx[c >> 1]);
-        sc[j][c] = p;
-        ls[c >> 1] += p;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * corr[r] + ls[r];
-#pragma unroll
-    for (int nt = 0; nt < NT_D; ++nt) {
-      o[nt][0] *= corr[0];
-      o[nt][1] *= corr[0];
-      o[nt][2] *= corr[1];
-      o[nt][3] *= corr[1];
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        const int mi = lane >> 3;
-        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
-        const int d = dp * 16 + (mi >> 1) * 8;
-        uint32_t b[4];
-        ldsm_x4_trans(kv_addr(vb, key, d), b);
-        mma_bf16_16816(o[2 * dp], pa, b[0], b[1]);
-        mma_bf16_16816(o[2 * dp + 1], pa, b[2], b[3]);
-      }
-    }
+    fa_tile<D>(fa, kb, kb + TILE_BYTES, (t0 + i) * KT, nkeys, P.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (threadIdx.x == 0 && i + STAGES < n) {
@@ -261,28 +135,23 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   }
 
   if (threadIdx.x == 0) tl_stamp(tl, 7);
-  // row sums across the quad
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-  }
+  fa_end<D>(fa);
   __syncthreads();  // the ring is free: every issued tile was consumed
   {
     const int ra = warp * 16 + r0, rb = ra + 8;
 #pragma unroll
     for (int nt = 0; nt < NT_D; ++nt) {
       const int d = nt * 8 + kq;
-      s_o[ra * D + d] = o[nt][0];
-      s_o[ra * D + d + 1] = o[nt][1];
-      s_o[rb * D + d] = o[nt][2];
-      s_o[rb * D + d + 1] = o[nt][3];
+      s_o[ra * D + d] = fa.o[nt][0];
+      s_o[ra * D + d + 1] = fa.o[nt][1];
+      s_o[rb * D + d] = fa.o[nt][2];
+      s_o[rb * D + d + 1] = fa.o[nt][3];
     }
     if ((lane & 3) == 0) {
-      s_m[ra] = m_run[0];
-      s_m[rb] = m_run[1];
-      s_l[ra] = l_run[0];
-      s_l[rb] = l_run[1];
+      s_m[ra] = fa.m[0];
+      s_m[rb] = fa.m[1];
+      s_l[ra] = fa.l[0];
+      s_l[rb] = fa.l[1];
     }
   }
   cluster_sync();
@@ -346,7 +215,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
                               static_cast<size_t>(g * nw + w) * D + d) = pk;
   }
   if (threadIdx.x == 0) tl_stamp(tl, 9);
-  if (threadIdx.x == 0) tl_stamp(tl, 20);
+  if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 

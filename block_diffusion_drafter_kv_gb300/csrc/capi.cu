@@ -147,7 +147,7 @@ struct dflash_handle {
   int device = 0;
   int n_sms = 0;
   int inject_pass_rows = 16;
-  int gemv_pref = 2;  // weight-streaming kernel variant for single-row-group launches
+  int gemv_pref = 3;  // weight-streaming kernel variant for single-row-group launches
   int chain_slot = 0;
   int chain_max = kMaxPhases;  // projections per persistent launch (1 = one launch per projection)
   // weight descriptors

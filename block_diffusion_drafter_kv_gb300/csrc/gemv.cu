@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         const uint32_t n = u1 > u0 ? u1 - u0 : 0;
         const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
         tl_stamp(tl, 4 + 4 * p);
+        if (n == 0 && p > 0) continue;  // nothing to load: run ahead to the next phase's weights
         uint32_t a_only = 0;  // weights do not depend on earlier phases: stream them first
         for (; a_only < pre; ++a_only) {
           const uint32_t i = it + a_only, s = i % C::STAGES, r = i / C::STAGES;
@@ -632,22 +633,29 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                 float v[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                for (int cc = ca; cc <= cb; cc += 2) {   // two segments' loads in flight per round
-                  const float* s0 = P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128;
-                  float a[16], b[16];
+                // partials summed in CTA order; up to 8 CTAs' loads in flight per round, JC rows
+                // of the chunk at a time (fewer where the register budget is halved)
+                constexpr int JC = C::MINB == 1 ? 8 : 4;
+                for (int cc0 = ca; cc0 <= cb; cc0 += 8) {
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) a[j] = __ldcg(s0 + (ch * 16 + j) * 128 + m);
-                  if (cc + 1 <= cb) {
-                    const float* s1 =
-                        P.part + static_cast<size_t>(part_slot(cc + 1, t, U, Gp, P.KB)) * C::ROWS * 128;
+                  for (int h = 0; h < 16 / JC; ++h) {
+                    float a[8][JC];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) b[j] = __ldcg(s1 + (ch * 16 + j) * 128 + m);
-                  }
+                    for (int q2 = 0; q2 < 8; ++q2) {
+                      if (cc0 + q2 <= cb) {
+                        const float* src = P.part +
+                                           static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                                           (ch * 16 + h * JC) * 128 + m;
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) v[j] += a[j];
-                  if (cc + 1 <= cb) {
+                        for (int j = 0; j < JC; ++j) a[q2][j] = __ldcg(src + j * 128);
+                      }
+                    }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] += b[j];
+                    for (int q2 = 0; q2 < 8; ++q2)
+                      if (cc0 + q2 <= cb) {
+#pragma unroll
+                        for (int j = 0; j < JC; ++j) v[h * JC + j] += a[q2][j];
+                      }
                   }
                 }
                 epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq);
@@ -726,7 +734,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
   if (threadIdx.x == 0) {  // the last CTA out clears the barrier counters for the next launch
-    tl_stamp(tl, 20);
+    tl_stamp(tl, kTlExit);
     __threadfence();
     if (atomicAdd(CH.exit_cnt, 1) == G - 1) {
       for (int p = 0; p < NP; ++p) CH.bar[p] = 0;
@@ -735,6 +743,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
     }
   }
 }
+
+constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA on sm_103
 
 template <class C>
 static int launch_cfg(const GemvChain& p, int n_ctas, cudaStream_t stream, bool pdl) {
@@ -767,7 +777,8 @@ static int set_attr() {
   X(6, 2, 1, 4, 2)              \
   X(7, 4, 1, 3, 2)              \
   X(8, 8, 1, 3, 2)              \
-  X(9, 16, 1, 2, 2)
+  X(9, 16, 1, 2, 2)              \
+  X(10, 1, 2, 4, 1)
 
 int gemv_variant(int nb, int pref) {
   if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 0;

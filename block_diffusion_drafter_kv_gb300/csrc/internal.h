@@ -87,7 +87,7 @@ struct GemvParams {
 // Up to kMaxPhases projections run back to back in one persistent launch: phase p+1 may
 // read what phase p wrote (grid barrier in between); weights of phase p+1 are streamed
 // before the barrier. Every CTA must be resident at once (grid <= SMs, one CTA per SM).
-constexpr int kMaxPhases = 4;
+constexpr int kMaxPhases = 8;
 struct GemvChain {
   GemvParams ph[kMaxPhases];
   int n_phases;
@@ -100,9 +100,10 @@ struct GemvChain {
 // Timeline record of one CTA (kTlWords 64-bit words, %globaltimer nanoseconds):
 //   [0] (kind << 32) | launch id   [1] SM id   [2] entry   [3] set-up done
 //   [4 + 4p] phase p: producer starts it   [5 + 4p] its input is ready (previous phase / kernel)
-//   [6 + 4p] first operand stage landed    [7 + 4p] epilogue done with it
-//   [20] exit
-constexpr int kTlWords = 21;
+//   [6 + 4p] first operand stage landed    [7 + 4p] epilogue done with it   (p < 8)
+//   [kTlExit] exit
+constexpr int kTlWords = 37;
+constexpr int kTlExit = kTlWords - 1;
 enum TlKind : int { TL_GEMV = 1, TL_ATTN = 2, TL_EMBED = 3, TL_VERIFY = 4 };
 
 // Kernel variant for nb activation row groups of 16 (1, 2, 4, 8 or 16); `pref` selects

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
       *reinterpret_cast<float4*>(P.trace + off + 4) = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
-  if (threadIdx.x == 0) tl_stamp(tl, 20);
+  if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
   __shared__ float red[8];
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
     const int oi = __shfl_down_sync(0xffffffffu, bi, o);
     better(bv, bi, ov, oi);
   }
-  if (threadIdx.x == 0) tl_stamp(tl, 20);
+  if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
   __shared__ float wv[8];
   __shared__ int wi[8];
   __shared__ int s_last;

@@ -196,14 +196,15 @@ int32_t dflash_last_launch_count(const dflash_handle* h);
  * outlive their use; the library does not own them. */
 int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events);
 
-/* Per-CTA timeline. `records` is a caller-owned device buffer of n_records records of 21
+/* Per-CTA timeline. `records` is a caller-owned device buffer of n_records records of 37
  * uint64 words (n_records = 0 turns it off). While on, every CTA of every later launch
  * fills one record with %globaltimer nanosecond stamps, until the buffer is full:
- *   [0] (kind << 32) | launch number (kind 1 weight-streaming chain, 2 attention,
- *       3 block embedding, 4 verification)   [1] SM id   [2] entry   [3] set-up done
+ *   [0] (kind << 32) | launch number (kind 1 chained projection/attention kernel,
+ *       2 standalone attention, 3 block embedding, 4 verification)   [1] SM id
+ *   [2] entry   [3] set-up done
  *   [4+4p] phase p started   [5+4p] its input ready   [6+4p] first operand landed
- *   [7+4p] phase p finished (p < 4; attention/embedding/verification fill [5] only)
- *   [20] exit
+ *   [7+4p] phase p finished (p < 8; other kernels fill [5] and a few of [6..9] only)
+ *   [36] exit
  * Unset stamps keep whatever the buffer held, so clear it first. Calling this again
  * restarts at record 0. Stamps cost a few instructions per CTA. */
 int dflash_timeline(dflash_handle* h, void* records, int64_t n_records);

@@ -119,6 +119,10 @@ def test_step_loop_matches_oracle(tiny, B):
     """Prefill injection, then 3 steps of draft -> (synthetic target) -> verify -> inject,
     compared with the oracle at every stage. Verification is fed the oracle's drafts so a
     legitimately different draft (top-2 gap < 1e-2) cannot desynchronise the two sides."""
+    _step_loop(tiny, B)
+
+
+def _step_loop(tiny, B):
     from gpu_util import check_draft, max_rel, LAYER_RTOL
     s, w = tiny.s, W_TINY
     d = tiny.drafter
