@@ -64,28 +64,33 @@ def peaks():
 
 def proj_bytes_flops(s, batch, B, tau):
     """Algorithmic (bytes, flops) of each projection: the weight read once, the activation
-    rows read once, the outputs written once."""
+    rows read once, the outputs written once. bf16 activation operands are two planes
+    (high and low, 4 bytes per value); q and the K cache are fp32, the V cache bf16; the
+    residual stream is fp32 (read and written by O and down). FLOPs count one product per
+    weight and row (the low plane's second product is not counted)."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     rows = batch * B
     kin = s.n_taps * s.target_hidden
-    kv = 2 * s.n_layers * s.n_kv_heads * d
+    kvd = s.n_kv_heads * d
+    kv = 2 * s.n_layers * kvd
     nqkv = (s.n_heads + 2 * s.n_kv_heads) * d
     nqd = s.n_heads * d
     return {
-        "fc": (2 * H * kin + 2 * tau * kin + 2 * tau * H, 2 * tau * H * kin),
-        "kv": (2 * kv * H + 2 * tau * H + 2 * tau * kv, 2 * tau * kv * H),
-        "qkv": (2 * nqkv * H + 2 * rows * (H + nqkv), 2 * rows * nqkv * H),
-        "o": (2 * H * nqd + 2 * rows * nqd + 4 * 2 * rows * H, 2 * rows * H * nqd),
-        "gateup": (2 * 2 * I * H + 2 * rows * (H + I), 2 * rows * 2 * I * H),
-        "down": (2 * H * I + 2 * rows * I + 4 * 2 * rows * H, 2 * rows * H * I),
-        "lm_head": (2 * V * H + 2 * rows * H + 4 * batch * (B - 1), 2 * batch * (B - 1) * V * H),
+        "fc": (2 * H * kin + 2 * tau * kin + 4 * tau * H, 2 * tau * H * kin),
+        "kv": (2 * kv * H + 4 * tau * H + 3 * tau * kv, 2 * tau * kv * H),
+        "qkv": (2 * nqkv * H + 4 * rows * H + rows * (4 * nqd + 6 * kvd), 2 * rows * nqkv * H),
+        "o": (2 * H * nqd + 4 * rows * nqd + 12 * rows * H, 2 * rows * H * nqd),
+        "gateup": (2 * 2 * I * H + 4 * rows * (H + I), 2 * rows * 2 * I * H),
+        "down": (2 * H * I + 4 * rows * I + 12 * rows * H, 2 * rows * H * I),
+        "lm_head": (2 * V * H + 4 * rows * H + 4 * batch * (B - 1), 2 * batch * (B - 1) * V * H),
     }
 
 
 def attn_bytes_flops(s, batch, B, n_ctx):
-    """KV read once per layer per sequence (context plus block keys), q read, o written."""
-    kvb = 2 * 2 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
-    qo = 2 * 2 * batch * B * s.n_heads * s.head_dim
+    """K (fp32) and V (bf16) read once per layer per sequence (context plus block keys),
+    q (fp32) read, o (two bf16 planes) written."""
+    kvb = 6 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
+    qo = 8 * batch * B * s.n_heads * s.head_dim
     fl = 4 * batch * B * s.n_heads * s.head_dim * (n_ctx + B)
     return kvb + qo, fl
 

@@ -10,9 +10,11 @@
 // Split-KV flash decoding: one thread-block cluster per (sequence, KV head); the CTAs of
 // the cluster split the key range. In a CTA, warp w serves query head g*group + w for all
 // (<= 16) block slots, so the group's query heads share every K/V tile staged in shared
-// memory by TMA. QKᵀ and PV run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate) with an online softmax in registers. The CTAs' partial (max, sum, output)
-// are merged through distributed shared memory in a fixed order, so no partials touch HBM.
+// memory by TMA. QKᵀ runs on the tensor cores in TF32 against the fp32 K cache and PV in
+// bf16 against the bf16 V cache, both accumulating in fp32, with an online softmax in
+// registers. The CTAs' partial (max, sum, output) are merged through distributed shared
+// memory in a fixed order, so no partials touch HBM. The output is written as a high bf16
+// plane and a low plane (the bf16 of the remainder) for the output projection.
 #include "attn_tile.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -34,12 +36,13 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     tl[1] = smid();
     tl_stamp(tl, 2);
   }
-  constexpr int TILE_BYTES = KT * D * 2;
-  constexpr int NBOX = D / 64;
+  constexpr int K_BYTES = KT * D * 4;  // fp32 K tile
+  constexpr int V_BYTES = KT * D * 2;  // bf16 V tile
+  constexpr int TILE_BYTES = K_BYTES + V_BYTES;
   constexpr int NT_D = D / 8;   // n-tiles over d in the output
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * 2 * TILE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
   uint64_t* empty = full + STAGES;
   float* s_m = reinterpret_cast<float*>(empty + STAGES);  // [128] per-row running max (log2 units)
   float* s_l = s_m + 128;                                  // [128] per-row sum
@@ -83,15 +86,14 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
 
   auto issue = [&](int i, uint64_t pol) {
     const int st = i % STAGES;
-    uint8_t* kd = smem + st * 2 * TILE_BYTES;
-    uint8_t* vd = kd + TILE_BYTES;
+    uint8_t* kd = smem + st * TILE_BYTES;
+    uint8_t* vd = kd + K_BYTES;
     const int row = key_row0 + (t0 + i) * KT;
-    mbar_arrive_expect_tx(&full[st], 2 * TILE_BYTES);
+    mbar_arrive_expect_tx(&full[st], TILE_BYTES);
 #pragma unroll
-    for (int b = 0; b < NBOX; ++b) {
-      tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
-      tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
-    }
+    for (int b = 0; b < D / 32; ++b) tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 32, g, row, pol);
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
   };
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_last();
@@ -121,8 +123,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
       raise_flag(P.err, kDevTimeout);
     }
     if (i == 0 && threadIdx.x == 0) tl_stamp(tl, 6);
-    const uint32_t kb = smem_u32(smem + st * 2 * TILE_BYTES);
-    fa_tile<D>(fa, kb, kb + TILE_BYTES, (t0 + i) * KT, nkeys, P.scale_log2, lane);
+    const uint32_t kb = smem_u32(smem + st * TILE_BYTES);
+    fa_tile<D>(fa, kb, kb + K_BYTES, (t0 + i) * KT, nkeys, P.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (threadIdx.x == 0 && i + STAGES < n) {
@@ -207,12 +209,18 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
         acc.z += wt * part[c].z;
         acc.w += wt * part[c].w;
       }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(P.o + (static_cast<size_t>(seq) * B + slot) * nq * D +
-                              static_cast<size_t>(g * nw + w) * D + d) = pk;
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(acc.x, acc.y), h23 = __floats2bfloat162_rn(acc.z, acc.w);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(acc.x - f01.x, acc.y - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(acc.z - f23.x, acc.w - f23.y);
+    uint2 ph, pl;
+    ph.x = *reinterpret_cast<const uint32_t*>(&h01);
+    ph.y = *reinterpret_cast<const uint32_t*>(&h23);
+    pl.x = *reinterpret_cast<const uint32_t*>(&l01);
+    pl.y = *reinterpret_cast<const uint32_t*>(&l23);
+    __nv_bfloat16* dst = P.o + (static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d;
+    *reinterpret_cast<uint2*>(dst) = ph;
+    *reinterpret_cast<uint2*>(dst + static_cast<size_t>(P.o_lo) * nq * D) = pl;
   }
   if (threadIdx.x == 0) tl_stamp(tl, 9);
   if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
@@ -221,7 +229,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
 
 template <int D>
 static int attn_smem() {
-  return 1024 + STAGES * 2 * (KT * D * 2) + STAGES * 16 + (128 * 2 + 128 * 16) * 4 + 16;
+  return 1024 + STAGES * (KT * D * 6) + STAGES * 16 + (128 * 2 + 128 * 16) * 4 + 16;
 }
 
 int attn_set_attributes() {

@@ -2,9 +2,13 @@
 // the attention phase of the chained projection kernel (sm_103a).
 //
 // One warp owns 16 query rows (the block's slots for one query head) and walks key tiles
-// of 64 staged in shared memory by TMA (128-byte swizzled boxes of 64 keys x 64 dims):
-// S = Q Kᵀ and O += P V on the tensor cores (mma.sync m16n8k16, bf16 inputs, fp32
-// accumulation) with an online softmax in registers, in log2 units.
+// of 64 staged in shared memory by TMA: K as fp32 (128-byte swizzled boxes of 64 keys x 32
+// dims), V as bf16 (boxes of 64 keys x 64 dims). S = Q Kᵀ runs on the tensor cores in TF32
+// (mma.sync m16n8k8; q and K are stored already rounded to TF32), because the scores are
+// the step's most rounding-sensitive quantity: the attention output is a weighted mean of
+// values with much cancellation, so small score errors grow in relative terms. O += P V
+// runs in bf16 (mma.sync m16n8k16), all accumulation in fp32, with an online softmax in
+// registers in log2 units.
 #pragma once
 
 #include "ptx.cuh"
@@ -30,39 +34,51 @@ DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+DEV void mma_tf32_1688(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte address of element (key, d) in a K or V tile: D/64 TMA boxes of 64 keys x 128 bytes,
+// Byte address of element (key, d) in a bf16 V tile: D/64 TMA boxes of 64 keys x 128 bytes,
 // each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
 DEV uint32_t kv_addr(uint32_t base, int key, int d) {
   const int box = d >> 6, dd = d & 63;
   return base + box * (kAttnKeys * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
 }
+// The same for an fp32 K tile: D/32 boxes of 64 keys x 128 bytes (32 dims); d a multiple of 4.
+DEV uint32_t k32_addr(uint32_t base, int key, int d) {
+  const int box = d >> 5, dd = d & 31;
+  return base + box * (kAttnKeys * 128) + key * 128 + ((((dd >> 2) ^ (key & 7))) << 4);
+}
 
 template <int D>
 struct FaState {
-  uint32_t qa[D / 16][4];  // Q fragments (A operand)
+  uint32_t qa[D / 8][4];   // Q fragments (TF32 A operand, one per 8 dims)
   float m[2], l[2];        // running max (log2 units) and sum for rows r0 and r0 + 8
   float o[D / 8][4];       // unnormalised output accumulators
 };
 
 // Q rows for one query head: row i (< B) is query[row0 + i][head*D .. +D); rows >= B are zero.
 template <int D>
-DEV void fa_begin(FaState<D>& st, const __nv_bfloat16* q, size_t row0, size_t ld, int head, int B, int lane) {
-  const int r0 = lane >> 2, kq = (lane & 3) * 2;
-  const __nv_bfloat16* q0 = q + (row0 + r0) * ld + static_cast<size_t>(head) * D;
-  const __nv_bfloat16* q1 = q0 + 8 * ld;
+DEV void fa_begin(FaState<D>& st, const float* q, size_t row0, size_t ld, int head, int B, int lane) {
+  const int r0 = lane >> 2, kc = lane & 3;
+  const float* q0 = q + (row0 + r0) * ld + static_cast<size_t>(head) * D;
+  const float* q1 = q0 + 8 * ld;
   const bool v0 = r0 < B, v1 = r0 + 8 < B;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const int c = kk * 16 + kq;
-    st.qa[kk][0] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c)) : 0u;
-    st.qa[kk][1] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(q1 + c)) : 0u;
-    st.qa[kk][2] = v0 ? __ldcg(reinterpret_cast<const unsigned int*>(q0 + c + 8)) : 0u;
-    st.qa[kk][3] = v1 ? __ldcg(reinterpret_cast<const unsigned int*>(q1 + c + 8)) : 0u;
+  for (int kk = 0; kk < D / 8; ++kk) {
+    const int c = kk * 8 + kc;
+    st.qa[kk][0] = v0 ? __float_as_uint(__ldcg(q0 + c)) : 0u;
+    st.qa[kk][1] = v1 ? __float_as_uint(__ldcg(q1 + c)) : 0u;
+    st.qa[kk][2] = v0 ? __float_as_uint(__ldcg(q0 + c + 4)) : 0u;
+    st.qa[kk][3] = v1 ? __float_as_uint(__ldcg(q1 + c + 4)) : 0u;
   }
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.f;
@@ -71,7 +87,7 @@ DEV void fa_begin(FaState<D>& st, const __nv_bfloat16* q, size_t row0, size_t ld
 }
 
 // One tile of 64 keys starting at key0 (keys >= nkeys are masked out); kb / vb are the
-// shared-memory addresses of the staged K and V tiles.
+// shared-memory addresses of the staged fp32 K and bf16 V tiles.
 template <int D>
 DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, float scale_log2, int lane) {
   constexpr int NT_D = D / 8;
@@ -79,17 +95,19 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
   float sc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+  // ldmatrix on 16-bit pairs hands lane t the 32-bit element (row t/4, column t%4) of each
+  // 8 x (4 x 32-bit) matrix: with rows = keys and columns = 4 dims, that is the TF32 B
+  // fragment (k = t%4, n = t/4). Matrices 0..3: dims d0, d0+4 (step kk), d0+8, d0+12 (kk+1).
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < D / 8; kk += 2) {
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      const int mi = lane >> 3;
-      const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
-      const int d = kk * 16 + (mi & 1) * 8;
+    for (int np = 0; np < 8; ++np) {
+      const int key = np * 8 + (lane & 7);
+      const int d = kk * 8 + (lane >> 3) * 4;
       uint32_t b[4];
-      ldsm_x4(kv_addr(kb, key, d), b);
-      mma_bf16_16816(sc[2 * np], st.qa[kk], b[0], b[1]);
-      mma_bf16_16816(sc[2 * np + 1], st.qa[kk], b[2], b[3]);
+      ldsm_x4(k32_addr(kb, key, d), b);
+      mma_tf32_1688(sc[np], st.qa[kk], b[0], b[1]);
+      mma_tf32_1688(sc[np], st.qa[kk + 1], b[2], b[3]);
     }
   }
   // scale to log2 units, mask keys past the end, online softmax

@@ -68,12 +68,13 @@ WsLayout layout_of(const dflash_config& c) {
   L.ss_fc = take((H / 128) * kMaxPassRows * 4);
   L.ss_x = take((H / 128) * R * 4);
   L.ss_emb = take(R * 4);
-  L.cfeat = take(static_cast<size_t>(kMaxPassRows) * H * 2);
+  // bf16 activation operands hold a high plane of R rows and then the low plane (x - hi)
+  L.cfeat = take(static_cast<size_t>(2 * kMaxPassRows) * H * 2);
   L.x = take(R * H * 4);
-  L.xg = take(R * H * 2);
-  L.q = take(R * nq * d * 2);
-  L.o = take(R * nq * d * 2);
-  L.act = take(R * I * 2);
+  L.xg = take(2 * R * H * 2);
+  L.q = take(R * nq * d * 4);
+  L.o = take(2 * R * nq * d * 2);
+  L.act = take(2 * R * I * 2);
   L.vpart_v = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
   L.vpart_i = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
   L.chain_bar = take(static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4);
@@ -118,7 +119,18 @@ bool enc3d_hidden(CUtensorMap* m, const void* base, uint64_t Ht, uint64_t rows, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One layer's cache bf16 [rows = max_batch*cap][nkv][d], box 64 (d) x 1 head x 64 keys.
+// One layer's fp32 K cache [rows = max_batch*cap][nkv][d], box 32 (d, 128 bytes) x 1 head x 64 keys.
+bool enc3d_cache_f32(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
+  cuuint64_t dims[3] = {d, nkv, rows};
+  cuuint64_t strides[2] = {d * 4, nkv * d * 4};
+  cuuint32_t box[3] = {32, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One layer's bf16 V cache [rows = max_batch*cap][nkv][d], box 64 (d) x 1 head x 64 keys.
 bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
   cuuint64_t dims[3] = {d, nkv, rows};
   cuuint64_t strides[2] = {d * 2, nkv * d * 2};
@@ -129,10 +141,10 @@ bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uin
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int nb_index(int nb) { return nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : nb == 8 ? 3 : 4; }
+int nb_index(int nb) { return nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : 3; }
 int nb_for_rows(int rows) {
   int nb = 1;
-  while (nb * 16 < rows && nb < 16) nb *= 2;
+  while (nb * 16 < rows && nb * 16 < kMaxPassRows) nb *= 2;
   return nb;
 }
 
@@ -155,13 +167,13 @@ struct dflash_handle {
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
   // bound state
   bool bound = false;
-  __nv_bfloat16* kc = nullptr;
+  float* kc = nullptr;
   __nv_bfloat16* vc = nullptr;
   int* len = nullptr;
   int* last_token = nullptr;
   uint8_t* ws = nullptr;
   WsLayout L{};
-  CUtensorMap m_xg[5]{}, m_cfeat[5]{}, m_act[5]{}, m_o[5]{};
+  CUtensorMap m_xg[4]{}, m_cfeat[4]{}, m_act[4]{}, m_o[4]{};  // by nb_index, over both planes
   std::vector<CUtensorMap> m_kcache, m_vcache;
   int last_launches = 0;
   std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
@@ -336,7 +348,7 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
   const auto& c = h->cfg;
   const WsLayout L = layout_of(c);
   if (workspace_bytes < L.total) return DFLASH_E_CAPACITY;
-  h->kc = static_cast<__nv_bfloat16*>(k_cache);
+  h->kc = static_cast<float*>(k_cache);
   h->vc = static_cast<__nv_bfloat16*>(v_cache);
   h->len = len;
   h->last_token = last_token;
@@ -359,19 +371,19 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
     return DFLASH_E_CUDA;
   const uint64_t H = c.hidden, d = c.head_dim;
   bool ok = true;
-  for (int k = 0; k < 5 && ok; ++k) {
+  for (int k = 0; k < 4 && ok; ++k) {
     const uint32_t box = 16u << k;
-    ok = enc2d(&h->m_xg[k], h->ws + L.xg, H, L.R, box) &&
-         enc2d(&h->m_cfeat[k], h->ws + L.cfeat, H, kMaxPassRows, box) &&
-         enc2d(&h->m_act[k], h->ws + L.act, c.intermediate, L.R, box) &&
-         enc2d(&h->m_o[k], h->ws + L.o, c.n_heads * d, L.R, box);
+    ok = enc2d(&h->m_xg[k], h->ws + L.xg, H, 2 * L.R, box) &&
+         enc2d(&h->m_cfeat[k], h->ws + L.cfeat, H, 2 * kMaxPassRows, box) &&
+         enc2d(&h->m_act[k], h->ws + L.act, c.intermediate, 2 * L.R, box) &&
+         enc2d(&h->m_o[k], h->ws + L.o, c.n_heads * d, 2 * L.R, box);
   }
   h->m_kcache.resize(c.n_layers);
   h->m_vcache.resize(c.n_layers);
   const size_t layer_elems = static_cast<size_t>(c.max_batch) * c.kv_capacity * c.n_kv_heads * d;
   for (int l = 0; l < c.n_layers && ok; ++l) {
     const uint64_t rows = static_cast<uint64_t>(c.max_batch) * c.kv_capacity;
-    ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
+    ok = enc3d_cache_f32(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
          enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, rows);
   }
   if (!ok) return DFLASH_E_CUDA;
@@ -420,6 +432,7 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
       P.gain = static_cast<const __nv_bfloat16*>(h->w.g_ctx);
       P.yb = h->at<__nv_bfloat16>(h->L.cfeat);
       P.yb_ld = H;
+      P.yb_lo = kMaxPassRows;
       P.ss_out = h->at<float>(h->L.ss_fc);
       P.ss_stride = kMaxPassRows;
     }
@@ -437,6 +450,7 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
       P.KB = H / 64;
       P.bmap = h->m_cfeat[nb_index(nb)];
       P.b_row0 = 0;
+      P.b_lo = kMaxPassRows;
       P.grow0 = row0;
       P.op = OP_KV;
       P.ss_in = h->at<float>(h->L.ss_fc);
@@ -484,6 +498,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     E.len = h->len;
     E.x = h->at<float>(h->L.x);
     E.xg = h->at<__nv_bfloat16>(h->L.xg);
+    E.xg_lo = R;
     E.ss = h->at<float>(h->L.ss_emb);
     E.trace = x_trace;
     E.err = h->at<int>(h->L.err);
@@ -501,6 +516,8 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     gemv_common(h, P);
     P.bmap = bmap;
     P.b_row0 = row0;
+    P.b_lo = R;  // every draft operand has its low plane R rows down
+    P.yb_lo = R;
     P.grow0 = row0;
     P.out_row0 = row0;
     P.ss_row0 = row0;
@@ -529,7 +546,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
       P.ss_parts = H / 128;
     }
     P.ss_stride = R;
-    P.yb = h->at<__nv_bfloat16>(h->L.q);
+    P.qf = h->at<float>(h->L.q);
     P.yb_ld = c.n_heads * d;
     P.rope_cos = h->at<float>(h->L.rope_cos);
     P.rope_sin = h->at<float>(h->L.rope_sin);
@@ -623,8 +640,9 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     AttnParams A{};
     A.kmap = h->m_kcache[l];
     A.vmap = h->m_vcache[l];
-    A.q = h->at<__nv_bfloat16>(h->L.q);
+    A.q = h->at<float>(h->L.q);
     A.o = h->at<__nv_bfloat16>(h->L.o);
+    A.o_lo = R;
     A.len = h->len;
     A.err = h->at<int>(h->L.err);
     A.B = block;

@@ -24,31 +24,62 @@
 
 namespace dfl {
 
-// NB: activation row groups of 16 (MMA N = 16*NB). KSUB: 64-wide k-boxes per pipeline
-// stage (a stage holds 128 weight rows x 64*KSUB k, so each weight row contributes
+// NB: activation row groups of 16 (ROWS = 16*NB rows per pass). KSUB: 64-wide k-boxes per
+// pipeline stage (a stage holds 128 weight rows x 64*KSUB k, so each weight row contributes
 // 128*KSUB contiguous bytes per stage). STAGES: depth of the shared-memory ring.
 // MINB: CTAs per SM the launch bounds are sized for.
+//
+// Activations are carried as two bf16 planes, x = hi + lo with hi = bf16(x) and
+// lo = bf16(x - hi), so that a bf16 tensor-core product sees x to about 16 significant
+// bits: the B tile of a k-box holds the ROWS high rows followed by the ROWS low rows, one
+// MMA of N = 2*ROWS multiplies both, and the epilogue adds the two halves of the fp32
+// accumulator. The weight bytes streamed are unchanged; the MMA work doubles, which costs
+// nothing while the kernel waits on HBM. Operands that are exact in bf16 (the target's
+// hidden states) are loaded as the high plane only, with an MMA of N = ROWS.
 template <int NB, int KSUB, int STAGES_, int MINB_>
 struct GemvCfg {
-  static constexpr int ROWS = 16 * NB;               // MMA N
+  static constexpr int ROWS = 16 * NB;                // activation rows of a pass
+  static constexpr int NCOL = 2 * ROWS;               // MMA N with both planes
   static constexpr int KS = KSUB;
   static constexpr int STAGES = STAGES_;
   static constexpr int MINB = MINB_;
   static constexpr int A_SUB = 128 * 64 * 2;          // one 128 x 64 weight sub-tile (16 KB)
-  static constexpr int B_SUB = ROWS * 64 * 2;         // one ROWS x 64 activation sub-tile
+  static constexpr int B_PLANE = ROWS * 64 * 2;       // one plane of a ROWS x 64 activation sub-tile
+  static constexpr int B_SUB = 2 * B_PLANE;           // both planes
   static constexpr int A_BYTES = KSUB * A_SUB;
   static constexpr int B_BYTES = KSUB * B_SUB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int TMEM_COLS = 2 * ROWS < 32 ? 32 : 2 * ROWS;
+  static constexpr int TMEM_COLS = 2 * NCOL;          // two accumulators (power of two >= 64)
   static constexpr int XLD = 132;                     // padded row of the exchange buffer
   static constexpr int EPI_BYTES = 16 * XLD * 4 + 5 * ROWS * 4;  // xch, inv, best v/i, row pos/seq
   static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(128, ROWS);
+  static constexpr uint32_t IDESC2 = idesc_bf16_f32(128, NCOL);  // high and low planes
+  static constexpr uint32_t IDESC1 = idesc_bf16_f32(128, ROWS);  // high plane only
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(TMEM_COLS <= 512, "TMEM columns");
+  // CTAs of one persistent launch that can share an SM must fit in its TMEM together, or one
+  // would wait in tcgen05.alloc for columns held by a CTA that waits for it at a barrier.
+  static_assert((233472 / SMEM) * TMEM_COLS <= 512, "co-resident CTAs exceed TMEM");
 };
 
 DEV float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 DEV __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
+
+// Store v as a high bf16 at p and, when lo_off != 0, the bf16 of the remainder at p + lo_off.
+DEV void st_split(__nv_bfloat16* p, size_t lo_off, float v) {
+  const __nv_bfloat16 hi = f2bf(v);
+  p[0] = hi;
+  if (lo_off) p[lo_off] = f2bf(v - bf2f(hi));
+}
+
+// fp32 rounded to TF32 (10-bit mantissa, nearest, ties away), the operand precision of the
+// attention score MMA; values stored this way are used by it exactly.
+DEV float to_tf32(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return __uint_as_float(r);
+}
 
 // CTA whose unit range contains unit u (units split as floor(c*U/G)).
 DEV int cta_of_unit(uint32_t u, uint32_t U, int G) {
@@ -88,7 +119,9 @@ DEV void load_a(const GemvParams& P, int t, int ks, uint8_t* dst, uint64_t* bar,
   }
 }
 
-template <int KSUB, int B_SUB>
+// Activation sub-tiles of k-stage ks: per k-box the high plane, then (b_lo != 0) the low
+// plane b_lo rows further down the same map.
+template <int KSUB, int B_SUB, int B_PLANE>
 DEV void load_b(const GemvParams& P, int ks, uint8_t* dst, uint64_t* bar, uint64_t pol) {
 #pragma unroll
   for (int j = 0; j < KSUB; ++j) {
@@ -99,6 +132,7 @@ DEV void load_b(const GemvParams& P, int ks, uint8_t* dst, uint64_t* bar, uint64
       tma_load_3d(dst + j * B_SUB, &P.bmap, bar, col, P.b_row0, tap, pol);
     } else {
       tma_load_2d(dst + j * B_SUB, &P.bmap, bar, kb * 64, P.b_row0, pol);
+      if (P.b_lo) tma_load_2d(dst + j * B_SUB + B_PLANE, &P.bmap, bar, kb * 64, P.b_row0 + P.b_lo, pol);
     }
   }
 }
@@ -151,6 +185,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
                         const int* s_seq) {
   const int lr0 = chunk * 16;          // local row of v[0]
   const int gr0 = P.grow0 + lr0;       // global row of v[0]
+  const size_t lo_off = static_cast<size_t>(P.yb_lo) * P.yb_ld;  // low plane of yb (0: none)
   switch (P.op) {
     case OP_PLAIN: {
       const int n = t * 128 + m;
@@ -165,7 +200,8 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
       const int f = t * 128 + m;
       const float g = bf2f(P.gain[f]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) P.yb[static_cast<size_t>(P.out_row0 + lr0 + j) * P.yb_ld + f] = f2bf(v[j] * g);
+      for (int j = 0; j < 16; ++j)
+        st_split(P.yb + static_cast<size_t>(P.out_row0 + lr0 + j) * P.yb_ld + f, lo_off, v[j] * g);
       const float s = rows_sumsq(v, m, e, xch, XLD);
       if ((e & 7) == 0) P.ss_out[t * P.ss_stride + P.out_row0 + lr0 + (e >> 3)] = s;
     } break;
@@ -183,14 +219,14 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         pos[j] = max(s_pos[lr0 + j], 0);   // row positions were resolved once per phase
       }
       if (!is_v) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
-      __nv_bfloat16* cache = is_v ? P.vc : P.kc;
       const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (s_pos[lr0 + j] < 0) continue;
         const size_t off =
             ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
-        cache[off] = f2bf(val[j]);
+        if (is_v) P.vc[off] = f2bf(val[j]);
+        else P.kc[off] = to_tf32(val[j]);
       }
     } break;
 
@@ -208,16 +244,16 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
       if (mi == 0) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (gr0 + j < P.n_valid) P.yb[static_cast<size_t>(gr0 + j) * P.yb_ld + feat] = f2bf(val[j]);
+          if (gr0 + j < P.n_valid) P.qf[static_cast<size_t>(gr0 + j) * P.yb_ld + feat] = to_tf32(val[j]);
       } else {
-        __nv_bfloat16* cache = (mi == 1) ? P.kc : P.vc;
         const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (s_pos[lr0 + j] < 0) continue;
           const size_t off =
               ((static_cast<size_t>(P.layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
-          cache[off] = f2bf(val[j]);
+          if (mi == 1) P.kc[off] = to_tf32(val[j]);
+          else P.vc[off] = f2bf(val[j]);
         }
       }
     } break;
@@ -234,7 +270,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
           const size_t off = static_cast<size_t>(gr) * P.y_ld + f;
           const float xo = (NB == 1 ? xpre[j] : __ldcg(P.y + off)) + v[j];
           P.y[off] = xo;
-          P.yb[static_cast<size_t>(gr) * P.yb_ld + f] = f2bf(xo * g);
+          st_split(P.yb + static_cast<size_t>(gr) * P.yb_ld + f, lo_off, xo * g);
           if (P.trace) P.trace[off] = xo;
           w[j] = xo;
         }
@@ -258,7 +294,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
           const float gt = val[j];
           const float up = xch[j * XLD + m + 64];
           const float a = gt / (1.f + __expf(-gt)) * up;
-          if (gr0 + j < P.n_valid) P.yb[static_cast<size_t>(gr0 + j) * P.yb_ld + i] = f2bf(a);
+          if (gr0 + j < P.n_valid) st_split(P.yb + static_cast<size_t>(gr0 + j) * P.yb_ld + i, lo_off, a);
         }
       }
       named_bar_sync(1, 128);
@@ -417,6 +453,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         phase_units(P, c, G, U, u0, u1, Gp);
         const uint32_t n = u1 > u0 ? u1 - u0 : 0;
         const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
+        const uint32_t stage_bytes = C::A_BYTES + (P.b_lo ? 2 : 1) * C::KS * C::B_PLANE;
         tl_stamp(tl, 4 + 4 * p);
         if (n == 0 && p > 0) continue;  // nothing to load: run ahead to the next phase's weights
         uint32_t a_only = 0;  // weights do not depend on earlier phases: stream them first
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             break;
           }
           const uint32_t u = u0 + a_only;
-          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
           load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
         }
         bool dep_ok = ok;
@@ -445,7 +482,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         // every armed stage completes and the drain below cannot stall)
         for (uint32_t k = 0; k < a_only; ++k) {
           const uint32_t u = u0 + k, s = (it + k) % C::STAGES;
-          load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+          load_b<C::KS, C::B_SUB, C::B_PLANE>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
         }
         it += a_only;
         if (!ok || !dep_ok) {
@@ -459,9 +496,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             break;
           }
           const uint32_t u = u0 + k;
-          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
           load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
-          load_b<C::KS, C::B_SUB>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
+          load_b<C::KS, C::B_SUB, C::B_PLANE>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
           ++it;
         }
       }
@@ -495,7 +532,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem + acc * C::ROWS;
+          const uint32_t d_tmem = tmem + acc * C::NCOL;
+          const uint32_t idesc = P.b_lo ? C::IDESC2 : C::IDESC1;
           for (uint32_t u = ub; u < ue; ++u, ++i) {
             const uint32_t s = i % C::STAGES, r = i / C::STAGES;
             if (!mbar_wait(&full[s], r & 1)) {
@@ -511,7 +549,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32),
-                            smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), C::IDESC,
+                            smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), idesc,
                             (u > ub || j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&empty[s]);
           }
@@ -575,6 +613,17 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         }
       }
       named_bar_sync(1, 128);
+      const bool split = P.b_lo != 0;
+      // Accumulator of 16 rows (chunk ch): high-plane columns, plus the low-plane columns.
+      auto tmem_ld_acc = [&](uint32_t taddr, int ch, bool two, float (&v)[16]) {
+        tmem_ld16(taddr + ch * 16, v);
+        if (two) {
+          float w[16];
+          tmem_ld16(taddr + C::ROWS + ch * 16, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += w[j];
+        }
+      };
       if (u0 < u1) {
         for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
           const int acc = lt & 1;
@@ -596,11 +645,11 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           tc_fence_after();
           const int ca = cta_of_unit(static_cast<uint32_t>(t) * P.KB, U, Gp);
           const int cb = cta_of_unit(static_cast<uint32_t>(t + 1) * P.KB - 1, U, Gp);
-          const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ROWS;
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::NCOL;
           if (ca == cb) {
             for (int ch = 0; ch < NB; ++ch) {
               float v[16];
-              tmem_ld16(taddr + ch * 16, v);
+              tmem_ld_acc(taddr, ch, split, v);
               if (ch == NB - 1) {
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
@@ -612,7 +661,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
             for (int ch = 0; ch < NB; ++ch) {
               float v[16];
-              tmem_ld16(taddr + ch * 16, v);
+              tmem_ld_acc(taddr, ch, split, v);
 #pragma unroll
               for (int j = 0; j < 16; ++j) dst[(ch * 16 + j) * 128 + m] = v[j];
             }
@@ -769,20 +818,18 @@ static int set_attr() {
 // Kernel variants: row groups NB, k-boxes per stage, ring depth, CTAs per SM.
 #define DFL_GEMV_VARIANTS(X)   \
   X(0, 1, 1, 5, 2)              \
-  X(1, 1, 1, 11, 1)             \
+  X(1, 1, 1, 10, 1)             \
   X(2, 1, 2, 5, 1)              \
   X(3, 1, 4, 2, 1)              \
-  X(4, 1, 4, 3, 1)              \
+  X(4, 1, 2, 4, 1)              \
   X(5, 1, 2, 2, 2)              \
   X(6, 2, 1, 4, 2)              \
   X(7, 4, 1, 3, 2)              \
-  X(8, 8, 1, 3, 2)              \
-  X(9, 16, 1, 2, 2)              \
-  X(10, 1, 2, 4, 1)
+  X(8, 8, 1, 3, 1)
 
 int gemv_variant(int nb, int pref) {
-  if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 0;
-  return nb == 2 ? 6 : nb == 4 ? 7 : nb == 8 ? 8 : 9;
+  if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 3;
+  return nb == 2 ? 6 : nb == 4 ? 7 : 8;
 }
 
 int gemv_variant_ksub(int v) {

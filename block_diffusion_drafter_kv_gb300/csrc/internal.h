@@ -26,11 +26,12 @@ enum GemvOp : int {
 
 constexpr int kMaxAMaps = 16;
 constexpr int kMaxCtas = 256;      // workspace partial slots are sized for this many CTAs
-constexpr int kMaxPassRows = 256;  // activation rows per GEMM pass (MMA N <= 256)
+constexpr int kMaxPassRows = 128;  // activation rows per GEMM pass (MMA N = 2 x rows <= 256)
 
 struct GemvParams {
   CUtensorMap amap[kMaxAMaps];  // weight maps, box 64 (k) x 64 (rows), 128-byte swizzle
   CUtensorMap bmap;             // activation map, box 64 (k) x 16*NB rows [x 1 tap]
+  int b_lo;                     // rows from a high-plane row to its low plane in bmap; 0: no low plane
   int n_amaps;
   int tile_start[kMaxAMaps + 1];  // map i covers tiles [tile_start[i], tile_start[i+1])
   int pair_mode;                  // rows 0-63 of tile t from map 0 row 64t, rows 64-127 from map 1 row 64t
@@ -61,15 +62,17 @@ struct GemvParams {
   // outputs
   float* y;                 // PLAIN: Y; RESID: residual x
   int y_ld;
-  __nv_bfloat16* yb;        // FC: cfeat; RESID: xg; SWIGLU: act; QKV: q
+  __nv_bfloat16* yb;        // FC: cfeat; RESID: xg; SWIGLU: act (bf16 high plane)
   int yb_ld;
+  int yb_lo;                // rows from a yb row to its low plane; 0: write the high plane only
+  float* qf;                // QKV: post-RoPE queries, fp32 rounded to TF32, [rows][nq*d]
   float* trace;             // RESID: optional residual trace
   // RoPE and caches
   const float* rope_cos;    // [cap][d/2]
   const float* rope_sin;
   int d;
-  __nv_bfloat16* kc;        // [L][max_batch][cap][nkv][d]
-  __nv_bfloat16* vc;
+  float* kc;                // K cache, fp32 rounded to TF32: [L][max_batch][cap][nkv][d]
+  __nv_bfloat16* vc;        // V cache, bf16, same layout
   int nkv, cap, max_batch, layer;
   int* len;
   const int* n_new;
@@ -115,10 +118,11 @@ int gemv_set_attributes();
 
 // ---------------------------------------------------------------- block attention
 struct AttnParams {
-  CUtensorMap kmap;  // 3-D over this layer's K cache: {d, nkv, max_batch*cap}, box {64, 1, 64}
-  CUtensorMap vmap;
-  const __nv_bfloat16* q;  // [rows][nq*d], row = s*B + i, post-RoPE
-  __nv_bfloat16* o;        // [rows][nq*d]
+  CUtensorMap kmap;  // 3-D over this layer's fp32 K cache: {d, nkv, max_batch*cap}, box {32, 1, 64}
+  CUtensorMap vmap;  // 3-D over this layer's bf16 V cache: box {64, 1, 64}
+  const float* q;    // [rows][nq*d], row = s*B + i, post-RoPE, TF32-rounded
+  __nv_bfloat16* o;  // [rows][nq*d] high plane; the low plane follows o_lo rows further on
+  int o_lo;
   const int* len;
   int* err;
   int B, nq, nkv, d, cap;
@@ -137,7 +141,8 @@ struct EmbedParams {
   const int* last_token;
   const int* len;
   float* x;                       // [rows][H]
-  __nv_bfloat16* xg;              // [rows][H]
+  __nv_bfloat16* xg;              // [rows][H] high plane; low plane xg_lo rows further on
+  int xg_lo;
   float* ss;                      // [rows]
   float* trace;                   // [rows][H] or null
   int* err;

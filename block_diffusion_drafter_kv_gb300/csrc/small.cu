@@ -51,17 +51,20 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams P) {
     const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(&xs[it]);
     const __nv_bfloat16* gv = reinterpret_cast<const __nv_bfloat16*>(&gs[it]);
     float x[8];
-    __nv_bfloat16 xg[8];
+    __nv_bfloat16 xg[8], xl[8];  // x * gain as a high bf16 and the bf16 of its remainder
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       x[k] = __bfloat162float(xv[k]);
-      xg[k] = __float2bfloat16_rn(x[k] * __bfloat162float(gv[k]));
+      const float y = x[k] * __bfloat162float(gv[k]);
+      xg[k] = __float2bfloat16_rn(y);
+      xl[k] = __float2bfloat16_rn(y - __bfloat162float(xg[k]));
       ss += x[k] * x[k];
     }
     const size_t off = static_cast<size_t>(row) * P.H + f0;
     *reinterpret_cast<float4*>(P.x + off) = make_float4(x[0], x[1], x[2], x[3]);
     *reinterpret_cast<float4*>(P.x + off + 4) = make_float4(x[4], x[5], x[6], x[7]);
     *reinterpret_cast<uint4*>(P.xg + off) = *reinterpret_cast<const uint4*>(xg);
+    *reinterpret_cast<uint4*>(P.xg + off + static_cast<size_t>(P.xg_lo) * P.H) = *reinterpret_cast<const uint4*>(xl);
     if (P.trace) {
       *reinterpret_cast<float4*>(P.trace + off) = make_float4(x[0], x[1], x[2], x[3]);
       *reinterpret_cast<float4*>(P.trace + off + 4) = make_float4(x[4], x[5], x[6], x[7]);

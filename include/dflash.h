@@ -118,9 +118,12 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
 int dflash_destroy(dflash_handle* h);
 
 /* Bind caller-owned state:
- *   k_cache, v_cache  bf16 [L][max_batch][kv_capacity][nkv][d], zero-initialised by the
- *                     caller. K is stored after RoPE. Positions [len, len+B) are used as
- *                     scratch for the block's own keys/values during a draft.
+ *   k_cache           fp32 [L][max_batch][kv_capacity][nkv][d], K after RoPE, each value
+ *                     rounded to TF32 (10-bit mantissa): the attention scores are the
+ *                     step's most rounding-sensitive quantity and run as TF32 products.
+ *   v_cache           bf16 [L][max_batch][kv_capacity][nkv][d].
+ *                     Both zero-initialised by the caller. Positions [len, len+B) are used
+ *                     as scratch for the block's own keys/values during a draft.
  *   len               int32 [max_batch] injected positions per sequence (device)
  *   last_token        int32 [max_batch] slot-0 token of the next block (device)
  *   workspace         dflash_workspace_size(cfg) bytes, 256-byte aligned
@@ -176,7 +179,7 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
 
 /* Weight-streaming bf16 GEMM of the draft path, exposed for testing the engine alone:
  * Y[r][m] = sum_k X[r][k] * W[m][k] in fp32 accumulation.
- *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (rows <= 256),
+ *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (any rows; passes of 128),
  *   Y  fp32 [rows][n_out] out. Uses the handle's bound workspace for split-K partials. */
 int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K, const void* X,
                        int32_t rows, float* Y, void* stream);
