@@ -43,7 +43,8 @@ class Workload:
     gain_std: float = 0.1        # RMSNorm gains are 1 + N(0, gain_std)
 
     def with_block(self, block: int) -> "Workload":
-        return replace(self, block=block, name=f"{self.name}-B{block}")
+        base = self.name[: self.name.rfind("-B")] if "-B" in self.name else self.name
+        return replace(self, block=block, name=f"{base}-B{block}")
 
     def kv_capacity(self) -> int:
         """Positions a sequence's cache must hold: the longest ctx plus every
