@@ -155,19 +155,22 @@ DEV float rows_sumsq(const float (&w)[16], int m, int e, float* red, int XLD) {
   return s;
 }
 
-// Rotate-half RoPE across the tile: row m pairs with row m ^ (d/2) of the same head.
-DEV void rope16(float (&val)[16], const int (&pos)[16], int m, int d, const float* cosT, const float* sinT,
-                float* xch, int XLD) {
+// RoPE table entries of this thread's pair index for the 16 rows of a chunk.
+DEV void rope_tables16(const int (&pos)[16], int m, int d, const float* cosT, const float* sinT, float (&cs)[16],
+                       float (&sn)[16]) {
   const int half = d >> 1;
-  const int jh = m & (d - 1);
-  const int fi = jh & (half - 1);
-  const bool lo = jh < half;
-  float cs[16], sn[16];
+  const int fi = (m & (d - 1)) & (half - 1);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {  // table reads in flight while the exchange completes
+  for (int j = 0; j < 16; ++j) {
     cs[j] = __ldg(cosT + pos[j] * half + fi);
     sn[j] = __ldg(sinT + pos[j] * half + fi);
   }
+}
+
+// Rotate-half RoPE across the tile: row m pairs with row m ^ (d/2) of the same head.
+DEV void rope16(float (&val)[16], const float (&cs)[16], const float (&sn)[16], int m, int d, float* xch, int XLD) {
+  const int half = d >> 1;
+  const bool lo = (m & (d - 1)) < half;
 #pragma unroll
   for (int j = 0; j < 16; ++j) xch[j * XLD + m] = val[j];
   named_bar_sync(1, 128);
@@ -179,10 +182,18 @@ DEV void rope16(float (&val)[16], const int (&pos)[16], int m, int d, const floa
   named_bar_sync(1, 128);
 }
 
+// Per-tile epilogue inputs that do not depend on the accumulator, loaded before waiting for
+// it so that the epilogue after the MMAs has no dependent global loads (single row group).
+struct EpiPre {
+  bool have;
+  float g;                 // FC / RESID: gain of this thread's output feature
+  float cs[16], sn[16];    // KV / QKV: RoPE cos / sin at the chunk's row positions
+};
+
 template <int NB, int XLD>
 DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], int m, int e, float* xch,
                         const float* s_inv, float* s_bv, int* s_bi, const float (&xpre)[16], const int* s_pos,
-                        const int* s_seq) {
+                        const int* s_seq, const EpiPre& pre) {
   const int lr0 = chunk * 16;          // local row of v[0]
   const int gr0 = P.grow0 + lr0;       // global row of v[0]
   const size_t lo_off = static_cast<size_t>(P.yb_lo) * P.yb_ld;  // low plane of yb (0: none)
@@ -198,7 +209,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
 
     case OP_FC: {
       const int f = t * 128 + m;
-      const float g = bf2f(P.gain[f]);
+      const float g = pre.have ? pre.g : bf2f(P.gain[f]);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         st_split(P.yb + static_cast<size_t>(P.out_row0 + lr0 + j) * P.yb_ld + f, lo_off, v[j] * g);
@@ -218,7 +229,15 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         val[j] = v[j] * s_inv[lr0 + j];
         pos[j] = max(s_pos[lr0 + j], 0);   // row positions were resolved once per phase
       }
-      if (!is_v) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
+      if (!is_v) {
+        if (pre.have) {
+          rope16(val, pre.cs, pre.sn, m, P.d, xch, XLD);
+        } else {
+          float cs[16], sn[16];
+          rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, cs, sn);
+          rope16(val, cs, sn, m, P.d, xch, XLD);
+        }
+      }
       const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -240,7 +259,15 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
         val[j] = v[j] * s_inv[lr0 + j];
         pos[j] = max(s_pos[lr0 + j], 0);
       }
-      if (mi < 2) rope16(val, pos, m, P.d, P.rope_cos, P.rope_sin, xch, XLD);
+      if (mi < 2) {
+        if (pre.have) {
+          rope16(val, pre.cs, pre.sn, m, P.d, xch, XLD);
+        } else {
+          float cs[16], sn[16];
+          rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, cs, sn);
+          rope16(val, cs, sn, m, P.d, xch, XLD);
+        }
+      }
       if (mi == 0) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -260,7 +287,7 @@ DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], i
 
     case OP_RESID: {
       const int f = t * 128 + m;
-      const float g = bf2f(P.gain[f]);
+      const float g = pre.have ? pre.g : bf2f(P.gain[f]);
       float w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -635,6 +662,21 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                             ? __ldcg(P.y + static_cast<size_t>(P.grow0 + j) * P.y_ld + t * 128 + m)
                             : 0.f;
           }
+          EpiPre pre;
+          pre.have = NB == 1;
+          if (NB == 1) {
+            if (P.op == OP_RESID || P.op == OP_FC) {
+              pre.g = bf2f(P.gain[t * 128 + m]);
+            } else if (P.op == OP_KV || P.op == OP_QKV) {
+              const int mi = map_of_tile(P, t);
+              if (P.op == OP_KV ? !(mi & 1) : mi < 2) {
+                int pos[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pos[j] = max(s_pos[j], 0);
+                rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, pre.cs, pre.sn);
+              }
+            }
+          }
           if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
           named_bar_sync(1, 128);
           if (!s_misc[1 + acc]) {
@@ -654,7 +696,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
               }
-              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq);
+              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq, pre);
             }
           } else {
             const int slot = part_slot(c, t, U, Gp, P.KB);
@@ -683,8 +725,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;
                 // partials summed in CTA order; up to 8 CTAs' loads in flight per round, JC rows
-                // of the chunk at a time (fewer where the register budget is halved)
-                constexpr int JC = C::MINB == 1 ? 8 : 4;
+                // of the chunk at a time (all 16 unless the register budget is halved)
+                constexpr int JC = C::MINB == 1 ? 16 : 4;
                 for (int cc0 = ca; cc0 <= cb; cc0 += 8) {
 #pragma unroll
                   for (int h = 0; h < 16 / JC; ++h) {
@@ -707,7 +749,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                       }
                   }
                 }
-                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq);
+                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq, pre);
               }
             }
           }
