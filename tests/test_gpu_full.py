@@ -91,3 +91,87 @@ def test_full_size_step_matches_oracle(full):
     g_dr, g_lo, g_tr = _draft(full, B)
     ores = full.oracle.draft(st, B)
     check_draft(ores, g_dr, g_lo, g_tr)
+
+
+# ------------------------------------------------------------------ batched and long-context configs
+# Sequences are independent in every step of the path (projections act row by row,
+# attention within a sequence, verification per sequence), so at these sizes the oracle
+# checks sampled sequences of a full-size GPU run. Sequences the oracle does not check get
+# N(0,1) hidden states drawn on the device.
+
+def _run_sampled(w, seed, sampled, oracle_dtype=np.float64, chunk=4096):
+    from gpu_util import Setup, check_draft, max_rel, LAYER_RTOL
+    from oracle.dflash_ref import Oracle
+    s, B, batch = w.shape, w.block, w.batch
+    ctx = I.ragged_ctx(w, seed)
+    sampled = list(sampled(ctx))
+    cap = int(ctx.max()) + 64
+    S = Setup(w, seed=seed, max_batch=batch, kv_capacity=cap)
+    d = S.drafter
+    rps = int(ctx.max())
+    hid = torch.empty(s.n_taps, batch * rps, s.target_hidden, dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    hid.normal_(generator=g)
+    host = {}
+    for q in sampled:
+        h = I.make_hidden(s, int(ctx[q]) + B, seed, f"seq{q}")
+        host[q] = h
+        hid[:, q * rps: q * rps + int(ctx[q])] = h[:, : int(ctx[q])].cuda()
+    last = I.initial_tokens(batch, s.vocab, seed)
+    d.len.zero_()
+    d.inject(hid, rps, torch.as_tensor(ctx, dtype=torch.int32, device="cuda"), batch)
+    d.last_token[:batch] = torch.as_tensor(last, device="cuda")
+    torch.cuda.synchronize()
+    assert d.len[:batch].cpu().tolist() == ctx.tolist() and d.device_error() == 0
+    del hid
+    o = Oracle(s, S.bits, dtype=oracle_dtype)
+    states = {}
+    for q in sampled:
+        st = o.new_sequence(cap, int(last[q]))
+        bits = I.bf16_bits(host[q][:, : int(ctx[q])])
+        for r0 in range(0, int(ctx[q]), chunk):
+            o.inject(st, bits[:, r0: r0 + chunk])
+        states[q] = st
+        k, v = S.gpu_cache(q, int(ctx[q]))
+        for l in range(s.n_layers):
+            assert max_rel(k[l], st.k_cache[l][: st.length]) <= LAYER_RTOL, f"seq {q} K layer {l}"
+            assert max_rel(v[l], st.v_cache[l][: st.length]) <= LAYER_RTOL, f"seq {q} V layer {l}"
+    drafted = torch.full((batch, B - 1), -1, dtype=torch.int32, device="cuda")
+    logits = torch.full((batch, B - 1, s.vocab), float("nan"), device="cuda")
+    trace = torch.full((s.n_layers + 1, batch * B, s.hidden), float("nan"), device="cuda")
+    d.draft(batch, B, drafted, logits, trace)
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    dr = drafted.cpu().numpy()
+    ores = {}
+    for q in sampled:
+        ores[q] = o.draft(states[q], B)
+        check_draft(ores[q], dr[q], logits[q].cpu().numpy(), trace[:, q * B:(q + 1) * B].cpu().numpy())
+        dr[q] = ores[q].drafted
+    # verification of the whole batch; the sampled sequences against the oracle, bit-exact
+    noise = I.make_logit_noise(batch, B, s.vocab, seed, "full.logits").numpy()
+    mask = I.make_plant_mask(batch, B, I.per_seq_p(w, seed), seed, "full.plant")
+    T = I.plant_logits(noise, dr, mask)
+    acc = torch.full((batch,), -7, dtype=torch.int32, device="cuda")
+    com = torch.full((batch, B), -7, dtype=torch.int32, device="cuda")
+    d.verify(torch.as_tensor(T, device="cuda"), torch.as_tensor(dr, device="cuda"), batch, B, acc, com)
+    torch.cuda.synchronize()
+    for q in sampled:
+        r = o.verify(states[q], T[q], dr[q])
+        assert int(acc[q]) == r.accept_len
+        assert list(com[q, : r.accept_len].cpu().numpy()) == list(r.committed)
+        assert int(d.last_token[q]) == r.last_token
+
+
+def test_batched_ragged_sampled_sequences_match_oracle():
+    """Batch 32, context lengths uniform in [512, 8192], B = 16, per-sequence agreement
+    rates: the two shortest sequences against the oracle."""
+    from synth import W_BATCHED
+    _run_sampled(W_BATCHED, 31, lambda ctx: np.argsort(ctx, kind="stable")[:2])
+
+
+def test_long_context_llama_shaped_sequence_matches_oracle():
+    """Llama-3.1-8B-shaped drafter (8 layers, SwiGLU 14336, vocab 128256, theta 5e5), batch 4
+    at context 32768, B = 16: sequence 0 against the oracle in fp32."""
+    from synth import W_LLAMA
+    _run_sampled(W_LLAMA, 41, lambda ctx: [0], oracle_dtype=np.float32)
