@@ -95,32 +95,43 @@ def attn_bytes_flops(s, batch, B, n_ctx):
     return kvb + qo, fl
 
 
-def launch_plan(s, batch, B, tau, n_ctx, n_sms=152):
+def _passes(rows, width):
+    return [(r0, min(width, rows - r0)) for r0 in range(0, rows, width)]
+
+
+def launch_plan(s, batch, B, tau, n_ctx, n_sms=152, one_pass=False):
     """Launch order of one step by call: (label, kind, bytes, flops). kind "gemv" marks the
-    chained kernel (one launch runs up to DFLASH_CHAIN_MAX phases); attention is a launch of
-    its own between chains. Mirrors the library's grouping."""
-    pj = proj_bytes_flops(s, batch, B, tau)
-    ab = attn_bytes_flops(s, batch, B, n_ctx)
+    chained kernel (one launch runs up to DFLASH_CHAIN_MAX phases, for one pass of at most
+    128 rows); attention is a launch of its own between chains. Injection runs in passes of
+    a width fixed by max_batch * max_block. Mirrors the library's grouping. With one_pass
+    every projection covers all rows at once: the method's own traffic, each weight once."""
     chain_max = int(os.environ.get("DFLASH_CHAIN_MAX", "8"))
-    segments = [[("qkv", *pj["qkv"])]]
-    for l in range(s.n_layers):
-        tail = ("qkv", *pj["qkv"]) if l + 1 < s.n_layers else ("lm_head", *pj["lm_head"])
-        body = [("o", *pj["o"]), ("gateup", *pj["gateup"]), ("down", *pj["down"]), tail]
-        segments += ["attn", body]
+    ab = attn_bytes_flops(s, batch, B, n_ctx)
+    rows = batch * B
+    nb = 1
+    while nb * 16 < min(rows, 128):
+        nb *= 2
+    inject = []
+    for _, pr in _passes(rows, rows if one_pass else 16 * nb):   # tau accepted rows per sequence, padded to B
+        pj = proj_bytes_flops(s, 1, pr, tau * pr / B)
+        inject.append(("fc+kv", "gemv", *tuple(map(sum, zip(pj["fc"], pj["kv"])))))
     draft = [("embed", "small", 2 * s.hidden * batch * (1 + 6 * B), 0)]
+    segments = [["qkv"]]
+    for l in range(s.n_layers):
+        segments += ["attn", ["o", "gateup", "down", "qkv" if l + 1 < s.n_layers else "lm_head"]]
     for seg in segments:
         if seg == "attn":
             draft.append(("attn", "attn", *ab))
             continue
-        for i in range(0, len(seg), chain_max):
-            cur = seg[i:i + chain_max]
-            draft.append(("+".join(n for n, _, _ in cur), "gemv", sum(b for _, b, _ in cur),
-                          sum(f for _, _, f in cur)))
-    return {
-        "inject": [("fc+kv", "gemv", *tuple(map(sum, zip(pj["fc"], pj["kv"]))))],
-        "draft": draft,
-        "verify": [("verify", "small", 4 * batch * B * s.vocab, 0)],
-    }
+        for _, pr in _passes(rows, rows if one_pass else 128):
+            pj = proj_bytes_flops(s, 1, pr, 1)
+            if "lm_head" in seg:   # the LM head of a pass covers its rows' drafted slots
+                pj["lm_head"] = proj_bytes_flops(s, pr // B if pr >= B else 1, B, 1)["lm_head"]
+            for i in range(0, len(seg), chain_max):
+                cur = seg[i:i + chain_max]
+                draft.append(("+".join(cur), "gemv", sum(pj[n][0] for n in cur), sum(pj[n][1] for n in cur)))
+    return {"inject": inject, "draft": draft,
+            "verify": [("verify", "small", 4 * batch * B * s.vocab, 0)]}
 
 
 def measured_traffic(launch, workload):
@@ -142,8 +153,10 @@ def measured_traffic(launch, workload):
 
 
 def step_bytes_flops(s, batch, B, n_ctx, tau):
+    """Algorithmic bytes and FLOPs of one step: every weight read once, K/V read once per
+    layer, activations and logits once (however the library splits rows into passes)."""
     byt = fl = 0
-    for call in launch_plan(s, batch, B, tau, n_ctx).values():
+    for call in launch_plan(s, batch, B, tau, n_ctx, one_pass=True).values():
         for _, kind, b, f in call:
             byt += b
             fl += f
@@ -330,10 +343,13 @@ def run_cuda(a):
     torch.cuda.synchronize()
     log(f"[bench] weights ready in {time.time() - t_setup:.1f}s; prefill {ctx_max} positions x {batch}")
     # prefill: inject the whole context of every sequence
-    hid_ctx = I.make_hidden(s, batch * ctx_max, a.seed + rank, "ctx")
+    # context hidden states N(0,1), drawn on the device from a seeded generator (up to
+    # 10 GB for the batched workload; the oracle's CPU baseline draws its own)
+    hid_ctx = torch.empty(s.n_taps, batch * ctx_max, s.target_hidden, dtype=torch.bfloat16, device="cuda")
+    hid_ctx.normal_(generator=torch.Generator(device="cuda").manual_seed(a.seed * 1000 + rank))
     n_ctx = torch.as_tensor(ctx_lens, dtype=torch.int32, device="cuda")
     with torch.cuda.stream(stream):
-        dr.inject(hid_ctx.cuda(), ctx_max, n_ctx, batch)
+        dr.inject(hid_ctx, ctx_max, n_ctx, batch)
         dr.last_token[:batch].copy_(torch.as_tensor(I.initial_tokens(batch, s.vocab, a.seed + rank)))
     stream.synchronize()
     del hid_ctx

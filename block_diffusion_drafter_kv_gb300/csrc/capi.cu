@@ -158,6 +158,9 @@ struct dflash_handle {
   std::vector<dflash_layer_weights> layers;
   int device = 0;
   int n_sms = 0;
+  // Rows per injection pass, fixed per handle (16 x the row groups of max_batch*max_block,
+  // at most 128): every injection then uses the same kernel variant and split of the
+  // weight, so a position's K/V are bit-identical however the positions are chunked.
   int inject_pass_rows = 16;
   int gemv_pref = 3;  // weight-streaming kernel variant for single-row-group launches
   int chain_slot = 0;
@@ -239,7 +242,7 @@ int run_chain_one(dflash_handle* h, const GemvParams* phases, int n, int nb, cud
   int ks = gemv_variant_ksub(v);
   for (int p = 0; p < n; ++p)
     if (phases[p].KB % ks != 0) {
-      v = gemv_variant(nb, 0);
+      v = gemv_variant_ksub1(nb);
       ks = gemv_variant_ksub(v);
     }
   for (int p = 0; p < n; ++p) {
@@ -305,6 +308,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->w = *w;
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
+  h->inject_pass_rows = 16 * nb_for_rows(std::min(cfg->max_batch * cfg->max_block, kMaxPassRows));
   if (const char* ev = std::getenv("DFLASH_GEMV_VARIANT")) h->gemv_pref = std::atoi(ev);
   if (const char* ev = std::getenv("DFLASH_CHAIN_MAX")) h->chain_max = std::max(1, std::min(kMaxPhases, std::atoi(ev)));
   if (cudaGetDevice(&h->device) != cudaSuccess ||
@@ -403,7 +407,7 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   call_begin(h, st);
   const int pass_rows = h->inject_pass_rows;
-  const int nb = pass_rows / 16;
+  const int nb = pass_rows / 16;  // a power of two by construction
   const int n_pass = ceil_div(total_rows, pass_rows);
   CUtensorMap m_hidden;
   if (!enc3d_hidden(&m_hidden, hidden, c.target_hidden, total_rows, c.n_taps, pass_rows)) return DFLASH_E_CUDA;

@@ -867,12 +867,20 @@ static int set_attr() {
   X(5, 1, 2, 2, 2)              \
   X(6, 2, 1, 4, 2)              \
   X(7, 4, 1, 3, 2)              \
-  X(8, 8, 1, 3, 1)
+  X(8, 8, 1, 3, 1)              \
+  X(9, 2, 4, 2, 1)              \
+  X(10, 4, 2, 3, 1)             \
+  X(11, 8, 2, 2, 1)
 
+// Several k-boxes per stage for every row count (contiguous bytes per weight row, and about
+// 128 KB of weights in flight per SM where shared memory allows); the 1-box variants 0 and
+// 6..8 serve phases whose k-block count the box count does not divide.
 int gemv_variant(int nb, int pref) {
   if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 3;
-  return nb == 2 ? 6 : nb == 4 ? 7 : 8;
+  return nb == 2 ? 9 : nb == 4 ? 10 : 11;
 }
+
+int gemv_variant_ksub1(int nb) { return nb == 1 ? 0 : nb == 2 ? 6 : nb == 4 ? 7 : 8; }
 
 int gemv_variant_ksub(int v) {
 #define DFL_KS(ID, NB, KS, ST, MB) if (v == ID) return KS;

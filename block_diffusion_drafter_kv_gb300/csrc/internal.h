@@ -113,6 +113,7 @@ enum TlKind : int { TL_GEMV = 1, TL_ATTN = 2, TL_EMBED = 3, TL_VERIFY = 4 };
 // among the nb == 1 variants. KB of a launch counts k-stages of 64 * gemv_variant_ksub(v).
 int gemv_variant(int nb, int pref);
 int gemv_variant_ksub(int variant);
+int gemv_variant_ksub1(int nb);  // the one-box-per-stage variant for nb
 int launch_gemv(const GemvChain& p, int variant, int n_ctas, cudaStream_t stream, bool pdl);
 int gemv_set_attributes();
 
