@@ -243,6 +243,28 @@ int attn_set_attributes() {
   return static_cast<int>(e);
 }
 
+// How many clusters of `split` CTAs of the head-dim-128 kernel the device can hold at once
+// (clusters above 8 CTAs need that many free SMs in one GPC); 0 if it cannot run one.
+int attn_resident_clusters(int split) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, 1, 1);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = attn_smem<128>();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<128>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 template <int D>
 static int launch_d(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl) {
   const int group = p.nq / p.nkv;

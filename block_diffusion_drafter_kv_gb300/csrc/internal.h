@@ -133,6 +133,7 @@ struct AttnParams {
 };
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
 int attn_set_attributes();
+int attn_resident_clusters(int split);
 
 // ---------------------------------------------------------------- small kernels
 struct EmbedParams {
