@@ -26,6 +26,12 @@ namespace {
 constexpr int KT = kAttnKeys;  // keys per tile
 constexpr int STAGES = 3;
 
+// Offset of the merge inputs from the 1024-aligned base: the ring of fp32 K + bf16 V tiles,
+// its full/empty barriers, the merge barrier and two flags.
+__host__ __device__ constexpr int attn_recv_offset(int D) {
+  return (STAGES * KT * D * 6 + (2 * STAGES + 1) * 8 + 8 + 15) / 16 * 16;
+}
+
 }  // namespace
 
 template <int D>
@@ -44,11 +50,10 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
   uint64_t* empty = full + STAGES;
-  float* s_m = reinterpret_cast<float*>(empty + STAGES);  // [128] per-row running max (log2 units)
-  float* s_l = s_m + 128;                                  // [128] per-row sum
-  float* s_w = s_l + 128;                                  // [128 rows][16] combine weights
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_w + 128 * 16);
-  float* s_o = reinterpret_cast<float*>(smem);             // [rows][D] after the key loop
+  uint64_t* recv_bar = empty + STAGES;  // the peers' partials of the rows this CTA merges
+  volatile int* s_flag = reinterpret_cast<volatile int*>(recv_bar + 1);  // [0] abort, [1] merge input ok
+  float* s_stage = reinterpret_cast<float*>(smem);  // after the key loop: partials by merging CTA
+  float* s_recv = reinterpret_cast<float*>(smem + attn_recv_offset(D));
 
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -56,20 +61,30 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   const int S = gridDim.x;
   const int rank = static_cast<int>(cluster_ctarank());
   const int B = P.B;
+  // The cluster's CTAs merge the nw*16 query rows in slices of `per` rows: rows [k*per,
+  // (k+1)*per) go to CTA k. CTA k receives from CTA c one block of partials at s_recv +
+  // c*nk*(D+4): its nk rows' outputs (D floats each), then their (max, sum, 0, 0).
+  const int R = nw * 16;
+  const int per = (R + S - 1) / S;
+  auto rows_of = [&](int k) { return max(0, min(per, R - k * per)); };
+  const int nrow = rows_of(rank);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nw);
     }
-    *s_abort = 0;
+    mbar_init(recv_bar, 1);
+    s_flag[0] = 0;
     fence_mbar_init();
+    mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S * nrow * (D + 4) * 4));
   }
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&P.kmap);
     tma_prefetch_desc(&P.vmap);
   }
   __syncthreads();
+  cluster_arrive_relaxed();  // peers may write this CTA's merge inputs once every CTA is here
 
   // The kernel before this one (the Q/K/V projection) starts only after the injection of
   // this step has completed, so len and the injected context keys [0, len) are final here;
@@ -118,8 +133,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
 
   for (int i = 0; i < n; ++i) {
     const int st = i % STAGES;
-    if (!*s_abort && !mbar_wait(&full[st], (i / STAGES) & 1)) {
-      *s_abort = 1;
+    if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1)) {
+      s_flag[0] = 1;
       raise_flag(P.err, kDevTimeout);
     }
     if (i == 0 && threadIdx.x == 0) tl_stamp(tl, 6);
@@ -128,11 +143,11 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (threadIdx.x == 0 && i + STAGES < n) {
-      if (!*s_abort && !mbar_wait(&empty[st], (i / STAGES) & 1)) {
-        *s_abort = 1;
+      if (!s_flag[0] && !mbar_wait(&empty[st], (i / STAGES) & 1)) {
+        s_flag[0] = 1;
         raise_flag(P.err, kDevTimeout);
       }
-      if (!*s_abort) issue(i + STAGES, policy_evict_last());
+      if (!s_flag[0]) issue(i + STAGES, policy_evict_last());
     }
   }
 
@@ -140,103 +155,108 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   fa_end<D>(fa);
   __syncthreads();  // the ring is free: every issued tile was consumed
   {
+    // stage this CTA's partial output and (max, sum) of every row in the ring, in one block
+    // per merging CTA k: [rows of k: D floats each][rows of k: (max, sum, 0, 0)]
     const int ra = warp * 16 + r0, rb = ra + 8;
+    auto stage_row = [&](int rr, int hi) {
+      const int k = rr / per, lr = rr - k * per;
+      float* blk = s_stage + static_cast<size_t>(k) * per * (D + 4);
 #pragma unroll
-    for (int nt = 0; nt < NT_D; ++nt) {
-      const int d = nt * 8 + kq;
-      s_o[ra * D + d] = fa.o[nt][0];
-      s_o[ra * D + d + 1] = fa.o[nt][1];
-      s_o[rb * D + d] = fa.o[nt][2];
-      s_o[rb * D + d + 1] = fa.o[nt][3];
-    }
-    if ((lane & 3) == 0) {
-      s_m[ra] = fa.m[0];
-      s_m[rb] = fa.m[1];
-      s_l[ra] = fa.l[0];
-      s_l[rb] = fa.l[1];
-    }
+      for (int nt = 0; nt < NT_D; ++nt)
+        *reinterpret_cast<float2*>(blk + lr * D + nt * 8 + kq) = make_float2(fa.o[nt][2 * hi], fa.o[nt][2 * hi + 1]);
+      if ((lane & 3) == 0)
+        *reinterpret_cast<float4*>(blk + rows_of(k) * D + lr * 4) = make_float4(fa.m[hi], fa.l[hi], 0.f, 0.f);
+    };
+    stage_row(ra, 0);
+    stage_row(rb, 1);
   }
-  cluster_sync();
-
+  fence_async_shared();  // the bulk copies below read the staged partials
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster has started and armed its merge barrier
+  if (warp == 0 && lane < S) {  // one bulk copy per merging CTA, each from its own lane
+    const int k = lane, nk = rows_of(k);
+    if (nk > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(nk * (D + 4) * 4);
+      const uint32_t src = smem_u32(s_stage) + static_cast<uint32_t>(k * per * (D + 4) * 4);
+      const uint32_t dst = smem_u32(s_recv) + static_cast<uint32_t>(rank * nk * (D + 4) * 4);
+      bulk_copy_to_peer(map_shared_rank(dst, k), src, bytes, map_shared_rank(smem_u32(recv_bar), k));
+    }
+    bulk_commit();
+  }
   if (threadIdx.x == 0) tl_stamp(tl, 8);
-  // merge: this CTA owns rows [rb0, rb1) of the nw*16 query rows. First every (row, split)
-  // pair's max and sum are fetched in parallel, then each row's split weights are formed.
-  const int R = nw * 16;
-  const int per = (R + S - 1) / S;
-  const int rb0 = rank * per, rb1 = min(R, rb0 + per);
-  const int nrow = max(rb1 - rb0, 0);
-  float* s_wm = s_w;              // [rows][S] remote maxima, then weights (rows*S <= 144)
-  float* s_wl = s_w + 1024;       // [rows][S] remote sums
-  for (int k = threadIdx.x; k < nrow * S; k += blockDim.x) {
-    const int rr = rb0 + k / S, c = k % S;
-    s_wm[(rr - rb0) * S + c] = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_m[rr]), c));
-    s_wl[(rr - rb0) * S + c] = ld_shared_cluster_f32(map_shared_rank(smem_u32(&s_l[rr]), c));
-  }
-  __syncthreads();
-  for (int k = threadIdx.x; k < nrow; k += blockDim.x) {
-    float M = -INFINITY;
-    for (int c = 0; c < S; ++c) M = fmaxf(M, s_wm[k * S + c]);
-    float den = 0.f;
-    for (int c = 0; c < S; ++c) {
-      const float mc = s_wm[k * S + c];
-      const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
-      s_wm[k * S + c] = w;
-      den += w * s_wl[k * S + c];
+
+  // merge the rows [rank*per, rank*per + nrow): block c of s_recv came from CTA c
+  if (nrow > 0) {
+    if (threadIdx.x == 0) {
+      const bool ok = mbar_wait(recv_bar, 0);
+      if (!ok) raise_flag(P.err, kDevTimeout);
+      s_flag[1] = ok ? 1 : 0;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int c = 0; c < S; ++c) s_wm[k * S + c] *= inv;
-  }
-  __syncthreads();
-  // combine: a thread takes 4 consecutive d of one row and reads all splits' values at once
-  constexpr int kMaxSplit = 16;
-  const int items = nrow * (D / 4);
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int rr = rb0 + it / (D / 4), d = (it % (D / 4)) * 4;
-    const int w = rr >> 4, slot = rr & 15;
-    if (slot >= B) continue;
-    float4 part[kMaxSplit];
-    const uint32_t a = smem_u32(&s_o[rr * D + d]);
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c)
-      if (c < S) part[c] = ld_shared_cluster_v4(map_shared_rank(a, c));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c)
-      if (c < S) {
-        const float wt = s_wm[(rr - rb0) * S + c];
-        acc.x += wt * part[c].x;
-        acc.y += wt * part[c].y;
-        acc.z += wt * part[c].z;
-        acc.w += wt * part[c].w;
+    __syncthreads();
+    if (s_flag[1]) {
+      const int blk = nrow * (D + 4);
+      const int items = nrow * (D / 4);
+      for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int lr = it / (D / 4), d = (it % (D / 4)) * 4;
+        const int rr = rank * per + lr;
+        const int w = rr >> 4, slot = rr & 15;
+        if (slot >= B) continue;
+        // split weights exp2(m_c - M) / sum_c' exp2(m_c' - M) l_c', combined in CTA order
+        const float* ml = s_recv + nrow * D + lr * 4;
+        float M = -INFINITY;
+        for (int c = 0; c < S; ++c) M = fmaxf(M, ml[c * blk]);
+        float den = 0.f;
+        for (int c = 0; c < S; ++c) {
+          const float mc = ml[c * blk];
+          den += (mc == -INFINITY ? 0.f : exp2f(mc - M)) * ml[c * blk + 1];
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < S; ++c) {
+          const float mc = ml[c * blk];
+          const float wt = (mc == -INFINITY ? 0.f : exp2f(mc - M)) * inv;
+          const float4 part = *reinterpret_cast<const float4*>(s_recv + c * blk + lr * D + d);
+          acc.x += wt * part.x;
+          acc.y += wt * part.y;
+          acc.z += wt * part.z;
+          acc.w += wt * part.w;
+        }
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(acc.x, acc.y), h23 = __floats2bfloat162_rn(acc.z, acc.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(acc.x - f01.x, acc.y - f01.y);
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(acc.z - f23.x, acc.w - f23.y);
+        uint2 ph, pl;
+        ph.x = *reinterpret_cast<const uint32_t*>(&h01);
+        ph.y = *reinterpret_cast<const uint32_t*>(&h23);
+        pl.x = *reinterpret_cast<const uint32_t*>(&l01);
+        pl.y = *reinterpret_cast<const uint32_t*>(&l23);
+        __nv_bfloat16* dst =
+            P.o + (static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d;
+        *reinterpret_cast<uint2*>(dst) = ph;
+        *reinterpret_cast<uint2*>(dst + static_cast<size_t>(P.o_lo) * nq * D) = pl;
       }
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(acc.x, acc.y), h23 = __floats2bfloat162_rn(acc.z, acc.w);
-    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-    const __nv_bfloat162 l01 = __floats2bfloat162_rn(acc.x - f01.x, acc.y - f01.y);
-    const __nv_bfloat162 l23 = __floats2bfloat162_rn(acc.z - f23.x, acc.w - f23.y);
-    uint2 ph, pl;
-    ph.x = *reinterpret_cast<const uint32_t*>(&h01);
-    ph.y = *reinterpret_cast<const uint32_t*>(&h23);
-    pl.x = *reinterpret_cast<const uint32_t*>(&l01);
-    pl.y = *reinterpret_cast<const uint32_t*>(&l23);
-    __nv_bfloat16* dst = P.o + (static_cast<size_t>(seq) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d;
-    *reinterpret_cast<uint2*>(dst) = ph;
-    *reinterpret_cast<uint2*>(dst + static_cast<size_t>(P.o_lo) * nq * D) = pl;
+    }
   }
   if (threadIdx.x == 0) tl_stamp(tl, 9);
+  // the staged partials stay in place until the peers' copies have read them; every copy
+  // into this CTA's memory has landed (its merge barrier completed) or this CTA merges none
+  if (warp == 0 && lane < S) bulk_wait_read();
   if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
-  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-template <int D>
-static int attn_smem() {
-  return 1024 + STAGES * (KT * D * 6) + STAGES * 16 + (128 * 2 + 128 * 16) * 4 + 16;
+// Dynamic shared memory: the tile ring (which holds this CTA's staged partials after the
+// key loop), its barriers, and the merge inputs from every CTA of the cluster.
+static int attn_smem(int D, int nw, int split) {
+  const int R = nw * 16, per = (R + split - 1) / split;
+  return 1024 + attn_recv_offset(D) + split * per * (D + 4) * 4;
 }
+static int attn_smem_max(int D) { return attn_smem(D, 8, 16); }
 
 int attn_set_attributes() {
   cudaError_t e = cudaSuccess;
 #define DFL_ATTN_ATTR(D)                                                                                   \
   if (e == cudaSuccess)                                                                                    \
-    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem<D>()); \
+    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_max(D)); \
   if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   DFL_ATTN_ATTR(64) DFL_ATTN_ATTR(128)
 #undef DFL_ATTN_ATTR
@@ -249,7 +269,7 @@ int attn_resident_clusters(int split) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, 1, 1);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = attn_smem<128>();
+  cfg.dynamicSmemBytes = attn_smem_max(128);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = split;
@@ -271,7 +291,7 @@ static int launch_d(const AttnParams& p, int batch, int split, cudaStream_t stre
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, p.nkv, batch);
   cfg.blockDim = dim3(32 * group);
-  cfg.dynamicSmemBytes = attn_smem<D>();
+  cfg.dynamicSmemBytes = attn_smem(D, group, split);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -783,11 +783,21 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               const int r = r0 + (e >> 3), lane8 = e & 7;
               float bv = -INFINITY;
               int bi = 0x7fffffff;
-#pragma unroll 4
-              for (int cc = lane8; cc < G; cc += 8) {
-                const float ov = __ldcg(P.best_v + cc * kMaxPassRows + r);
-                const int oi = __ldcg(P.best_i + cc * kMaxPassRows + r);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+              // the CTAs' candidates for row r, 160 at a time (one round up to 160 CTAs): all
+              // loads of a round in flight at once, then compared in CTA order
+              constexpr int kPer = 20;
+              for (int c0 = 0; c0 < G; c0 += 8 * kPer) {
+                float ov[kPer];
+                int oi[kPer];
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                  const int cc = c0 + lane8 + 8 * k;
+                  ov[k] = cc < G ? __ldcg(P.best_v + cc * kMaxPassRows + r) : -INFINITY;
+                  oi[k] = cc < G ? __ldcg(P.best_i + cc * kMaxPassRows + r) : 0x7fffffff;
+                }
+#pragma unroll
+                for (int k = 0; k < kPer; ++k)
+                  if (ov[k] > bv || (ov[k] == bv && oi[k] < bi)) { bv = ov[k]; bi = oi[k]; }
               }
 #pragma unroll
               for (int off = 4; off >= 1; off >>= 1) {
