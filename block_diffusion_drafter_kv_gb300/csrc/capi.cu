@@ -490,6 +490,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
   if (!h->bound) return DFLASH_E_STATE;
   const auto& c = h->cfg;
   if (batch < 1 || block < 1 || (block > 1 && !drafted)) return DFLASH_E_INVAL;
+  if (!aligned16(logits) || !aligned16(x_trace)) return DFLASH_E_INVAL;  // written 16 bytes at a time
   if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   call_begin(h, st);

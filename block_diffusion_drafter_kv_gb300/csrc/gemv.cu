@@ -66,12 +66,6 @@ struct GemvCfg {
 DEV float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 DEV __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
 
-// Store v as a high bf16 at p and, when lo_off != 0, the bf16 of the remainder at p + lo_off.
-DEV void st_split(__nv_bfloat16* p, size_t lo_off, float v) {
-  const __nv_bfloat16 hi = f2bf(v);
-  p[0] = hi;
-  if (lo_off) p[lo_off] = f2bf(v - bf2f(hi));
-}
 
 // fp32 rounded to TF32 (10-bit mantissa, nearest, ties away), the operand precision of the
 // attention score MMA; values stored this way are used by it exactly.
@@ -138,230 +132,304 @@ DEV void load_b(const GemvParams& P, int ks, uint8_t* dst, uint64_t* bar, uint64
 }
 
 // ---------------------------------------------------------------- epilogue helpers
-// Sum over the 128 tile rows of w[j]^2 for each of the 16 chunk rows; lane (e & 7) == 0 of
-// group j = e >> 3 gets row j's total. Fixed summation order.
-DEV float rows_sumsq(const float (&w)[16], int m, int e, float* red, int XLD) {
+// The epilogue works on one 16-row chunk of a 128-feature tile in the "row layout": thread
+// e holds row r = e / 8 and the 16 consecutive features c0 = (e % 8) * 16 .. c0 + 15, so
+// that every global load and store it makes is 16 bytes wide. (The accumulator arrives in
+// the column layout of tcgen05.ld, thread m = feature, 16 rows; to_rows transposes it.)
+struct RowPos {
+  int r, c0;
+};
+DEV RowPos row_pos(int e) { return {e >> 3, (e & 7) * 16}; }
+
+template <int XLD>
+DEV void to_rows(const float (&v)[16], int m, int e, float* xch, float (&o)[16]) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) red[j * XLD + m] = w[j] * w[j];
+  for (int j = 0; j < 16; ++j) xch[j * XLD + m] = v[j];
   named_bar_sync(1, 128);
-  const int j = e >> 3, part = e & 7;
+  const RowPos rp = row_pos(e);
+#pragma unroll
+  for (int k = 0; k < 16; k += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(xch + rp.r * XLD + rp.c0 + k);
+    o[k] = q.x;
+    o[k + 1] = q.y;
+    o[k + 2] = q.z;
+    o[k + 3] = q.w;
+  }
+  named_bar_sync(1, 128);
+}
+
+DEV void ld16(const float* p, float (&o)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; k += 4) {
+    const float4 q = __ldcg(reinterpret_cast<const float4*>(p + k));
+    o[k] = q.x;
+    o[k + 1] = q.y;
+    o[k + 2] = q.z;
+    o[k + 3] = q.w;
+  }
+}
+DEV void st16(float* p, const float (&v)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; k += 4) *reinterpret_cast<float4*>(p + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+}
+// 16 values as bf16 at p and, when lo_off != 0, the bf16 of the remainders at p + lo_off.
+DEV void st16_split(__nv_bfloat16* p, size_t lo_off, const float (&v)[16]) {
+  uint4 hi[2], lo[2];
+  __nv_bfloat16* hv = reinterpret_cast<__nv_bfloat16*>(hi);
+  __nv_bfloat16* lv = reinterpret_cast<__nv_bfloat16*>(lo);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    hv[k] = f2bf(v[k]);
+    lv[k] = f2bf(v[k] - bf2f(hv[k]));
+  }
+  reinterpret_cast<uint4*>(p)[0] = hi[0];
+  reinterpret_cast<uint4*>(p)[1] = hi[1];
+  if (lo_off) {
+    reinterpret_cast<uint4*>(p + lo_off)[0] = lo[0];
+    reinterpret_cast<uint4*>(p + lo_off)[1] = lo[1];
+  }
+}
+DEV void ld16_bf16(const __nv_bfloat16* p, float (&o)[16]) {
+  uint4 q[2];
+  q[0] = reinterpret_cast<const uint4*>(p)[0];
+  q[1] = reinterpret_cast<const uint4*>(p)[1];
+  const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(q);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) o[k] = bf2f(b[k]);
+}
+
+// Sum of squares of a row's 128 features: each lane sums its 16 in order, then the row's
+// 8 lanes combine in a fixed tree; lane (e % 8) == 0 holds the total.
+DEV float row_sumsq(const float (&w)[16]) {
   float s = 0.f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) s += red[j * XLD + part * 16 + k];
+  for (int k = 0; k < 16; ++k) s += w[k] * w[k];
   s += __shfl_down_sync(0xffffffffu, s, 4, 8);
   s += __shfl_down_sync(0xffffffffu, s, 2, 8);
   s += __shfl_down_sync(0xffffffffu, s, 1, 8);
-  named_bar_sync(1, 128);
   return s;
 }
 
-// RoPE table entries of this thread's pair index for the 16 rows of a chunk.
-DEV void rope_tables16(const int (&pos)[16], int m, int d, const float* cosT, const float* sinT, float (&cs)[16],
-                       float (&sn)[16]) {
+// RoPE table entries of a row position for this lane's 16 consecutive pair indices.
+DEV void rope_tables_row(int pos, int c0, int d, const float* cosT, const float* sinT, float (&cs)[16],
+                         float (&sn)[16]) {
   const int half = d >> 1;
-  const int fi = (m & (d - 1)) & (half - 1);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    cs[j] = __ldg(cosT + pos[j] * half + fi);
-    sn[j] = __ldg(sinT + pos[j] * half + fi);
-  }
+  const int fi0 = (c0 & (d - 1)) & (half - 1);
+  ld16(cosT + static_cast<size_t>(pos) * half + fi0, cs);
+  ld16(sinT + static_cast<size_t>(pos) * half + fi0, sn);
 }
 
-// Rotate-half RoPE across the tile: row m pairs with row m ^ (d/2) of the same head.
-DEV void rope16(float (&val)[16], const float (&cs)[16], const float (&sn)[16], int m, int d, float* xch, int XLD) {
+// Rotate-half RoPE on a row: feature c pairs with c ^ (d/2) of the same head, which lives
+// in lane (e % 8) ^ (d/32) of the same row group.
+DEV void rope_row(float (&val)[16], const float (&cs)[16], const float (&sn)[16], int c0, int d) {
   const int half = d >> 1;
-  const bool lo = (m & (d - 1)) < half;
+  const bool lo = (c0 & (d - 1)) < half;
+  const int lx = half >> 4;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) xch[j * XLD + m] = val[j];
-  named_bar_sync(1, 128);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float p = xch[j * XLD + (m ^ half)];
-    val[j] = lo ? (val[j] * cs[j] - p * sn[j]) : (val[j] * cs[j] + p * sn[j]);
+  for (int k = 0; k < 16; ++k) {
+    const float p = __shfl_xor_sync(0xffffffffu, val[k], lx, 8);
+    val[k] = lo ? (val[k] * cs[k] - p * sn[k]) : (val[k] * cs[k] + p * sn[k]);
   }
-  named_bar_sync(1, 128);
 }
 
 // Per-tile epilogue inputs that do not depend on the accumulator, loaded before waiting for
 // it so that the epilogue after the MMAs has no dependent global loads (single row group).
 struct EpiPre {
   bool have;
-  float g;                 // FC / RESID: gain of this thread's output feature
-  float cs[16], sn[16];    // KV / QKV: RoPE cos / sin at the chunk's row positions
+  float g[16];             // FC / RESID: gains of the lane's 16 features
+  float x[16];             // RESID: the residual the tile updates (lane's row and features)
+  float cs[16], sn[16];    // KV / QKV: RoPE cos / sin at the lane's row position
 };
 
-template <int NB, int XLD>
-DEV void epilogue_apply(const GemvParams& P, int t, int chunk, float (&v)[16], int m, int e, float* xch,
-                        const float* s_inv, float* s_bv, int* s_bi, const float (&xpre)[16], const int* s_pos,
-                        const int* s_seq, const EpiPre& pre) {
-  const int lr0 = chunk * 16;          // local row of v[0]
-  const int gr0 = P.grow0 + lr0;       // global row of v[0]
+template <int NB, int MINB>
+DEV void epilogue_prefetch(const GemvParams& P, int t, int e, const int* s_pos, EpiPre& pre) {
+  pre.have = NB == 1 && MINB == 1;  // a halved register budget cannot hold them across the wait
+  if (!pre.have) return;
+  const RowPos rp = row_pos(e);
+  if (P.op == OP_RESID || P.op == OP_FC) {
+    ld16_bf16(P.gain + t * 128 + rp.c0, pre.g);
+    if (P.op == OP_RESID) {
+      const int gr = P.grow0 + rp.r;
+      if (gr < P.n_valid) {
+        ld16(P.y + static_cast<size_t>(gr) * P.y_ld + t * 128 + rp.c0, pre.x);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pre.x[k] = 0.f;
+      }
+    }
+  } else if (P.op == OP_KV || P.op == OP_QKV) {
+    const int mi = map_of_tile(P, t);
+    if (P.op == OP_KV ? !(mi & 1) : mi < 2)
+      rope_tables_row(max(s_pos[rp.r], 0), rp.c0, P.d, P.rope_cos, P.rope_sin, pre.cs, pre.sn);
+  }
+}
+
+// Epilogue of rows [chunk*16, chunk*16 + 16) of tile t, v in the row layout.
+template <int NB>
+DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], int e, const float* s_inv,
+                       float* s_bv, int* s_bi, const int* s_pos, const int* s_seq, const EpiPre& pre) {
+  const RowPos rp = row_pos(e);
+  const int lr = chunk * 16 + rp.r;    // local row
+  const int gr = P.grow0 + lr;          // global row
+  const int c0 = rp.c0;
   const size_t lo_off = static_cast<size_t>(P.yb_lo) * P.yb_ld;  // low plane of yb (0: none)
   switch (P.op) {
     case OP_PLAIN: {
-      const int n = t * 128 + m;
-      if (n < P.n_out) {
+      if (gr < P.n_valid) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (gr0 + j < P.n_valid) P.y[static_cast<size_t>(P.out_row0 + lr0 + j) * P.y_ld + n] = v[j];
+        for (int k = 0; k < 16; ++k) {
+          const int n = t * 128 + c0 + k;
+          if (n < P.n_out) P.y[static_cast<size_t>(P.out_row0 + lr) * P.y_ld + n] = v[k];
+        }
       }
     } break;
 
     case OP_FC: {
-      const int f = t * 128 + m;
-      const float g = pre.have ? pre.g : bf2f(P.gain[f]);
+      float g[16], w[16];
+      if (pre.have) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        st_split(P.yb + static_cast<size_t>(P.out_row0 + lr0 + j) * P.yb_ld + f, lo_off, v[j] * g);
-      const float s = rows_sumsq(v, m, e, xch, XLD);
-      if ((e & 7) == 0) P.ss_out[t * P.ss_stride + P.out_row0 + lr0 + (e >> 3)] = s;
+        for (int k = 0; k < 16; ++k) g[k] = pre.g[k];
+      } else {
+        ld16_bf16(P.gain + t * 128 + c0, g);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) w[k] = v[k] * g[k];
+      st16_split(P.yb + static_cast<size_t>(P.out_row0 + lr) * P.yb_ld + t * 128 + c0, lo_off, w);
+      const float s = row_sumsq(v);
+      if ((e & 7) == 0) P.ss_out[t * P.ss_stride + P.out_row0 + lr] = s;
     } break;
 
-    case OP_KV: {
+    case OP_KV:
+    case OP_QKV: {
+      // KV: maps (Wk, Wv) per layer; QKV: 0 = q, 1 = k, 2 = v
       const int mi = map_of_tile(P, t);
-      const int layer = mi >> 1;
-      const bool is_v = mi & 1;
-      const int feat = (t - P.tile_start[mi]) * 128 + m;  // head*d + j within Wk / Wv
+      const bool is_q = P.op == OP_QKV && mi == 0;
+      const bool is_v = P.op == OP_KV ? (mi & 1) : mi == 2;
+      const int layer = P.op == OP_KV ? mi >> 1 : P.layer;
+      const int feat0 = (t - P.tile_start[mi]) * 128 + c0;  // head*d + j within the map
       float val[16];
-      int pos[16];
+      const float inv = s_inv[lr];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        val[j] = v[j] * s_inv[lr0 + j];
-        pos[j] = max(s_pos[lr0 + j], 0);   // row positions were resolved once per phase
-      }
+      for (int k = 0; k < 16; ++k) val[k] = v[k] * inv;
       if (!is_v) {
         if (pre.have) {
-          rope16(val, pre.cs, pre.sn, m, P.d, xch, XLD);
+          rope_row(val, pre.cs, pre.sn, c0, P.d);
         } else {
           float cs[16], sn[16];
-          rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, cs, sn);
-          rope16(val, cs, sn, m, P.d, xch, XLD);
+          rope_tables_row(max(s_pos[lr], 0), c0, P.d, P.rope_cos, P.rope_sin, cs, sn);
+          rope_row(val, cs, sn, c0, P.d);
         }
       }
-      const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
+      if (is_q) {
+        if (gr < P.n_valid) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (s_pos[lr0 + j] < 0) continue;
-        const size_t off =
-            ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
-        if (is_v) P.vc[off] = f2bf(val[j]);
-        else P.kc[off] = to_tf32(val[j]);
-      }
-    } break;
-
-    case OP_QKV: {
-      const int mi = map_of_tile(P, t);  // 0 = q, 1 = k, 2 = v
-      const int feat = (t - P.tile_start[mi]) * 128 + m;
-      float val[16];
-      int pos[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        val[j] = v[j] * s_inv[lr0 + j];
-        pos[j] = max(s_pos[lr0 + j], 0);
-      }
-      if (mi < 2) {
-        if (pre.have) {
-          rope16(val, pre.cs, pre.sn, m, P.d, xch, XLD);
-        } else {
-          float cs[16], sn[16];
-          rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, cs, sn);
-          rope16(val, cs, sn, m, P.d, xch, XLD);
+          for (int k = 0; k < 16; ++k) val[k] = to_tf32(val[k]);
+          st16(P.qf + static_cast<size_t>(gr) * P.yb_ld + feat0, val);
         }
-      }
-      if (mi == 0) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (gr0 + j < P.n_valid) P.qf[static_cast<size_t>(gr0 + j) * P.yb_ld + feat] = to_tf32(val[j]);
-      } else {
+      } else if (s_pos[lr] >= 0) {
         const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
+        const size_t off =
+            ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr]) * P.cap + s_pos[lr]) * row_elems + feat0;
+        if (is_v) {
+          uint4 b[2];
+          __nv_bfloat16* bv = reinterpret_cast<__nv_bfloat16*>(b);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (s_pos[lr0 + j] < 0) continue;
-          const size_t off =
-              ((static_cast<size_t>(P.layer) * P.max_batch + s_seq[lr0 + j]) * P.cap + pos[j]) * row_elems + feat;
-          if (mi == 1) P.kc[off] = to_tf32(val[j]);
-          else P.vc[off] = f2bf(val[j]);
+          for (int k = 0; k < 16; ++k) bv[k] = f2bf(val[k]);
+          reinterpret_cast<uint4*>(P.vc + off)[0] = b[0];
+          reinterpret_cast<uint4*>(P.vc + off)[1] = b[1];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) val[k] = to_tf32(val[k]);
+          st16(P.kc + off, val);
         }
       }
     } break;
 
     case OP_RESID: {
-      const int f = t * 128 + m;
-      const float g = pre.have ? pre.g : bf2f(P.gain[f]);
-      float w[16];
+      float xo[16], g[16];
+      if (pre.have) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int gr = gr0 + j;
-        w[j] = 0.f;
+        for (int k = 0; k < 16; ++k) {
+          xo[k] = pre.x[k];
+          g[k] = pre.g[k];
+        }
+      } else {
+        ld16_bf16(P.gain + t * 128 + c0, g);
         if (gr < P.n_valid) {
-          const size_t off = static_cast<size_t>(gr) * P.y_ld + f;
-          const float xo = (NB == 1 ? xpre[j] : __ldcg(P.y + off)) + v[j];
-          P.y[off] = xo;
-          st_split(P.yb + static_cast<size_t>(gr) * P.yb_ld + f, lo_off, xo * g);
-          if (P.trace) P.trace[off] = xo;
-          w[j] = xo;
+          ld16(P.y + static_cast<size_t>(gr) * P.y_ld + t * 128 + c0, xo);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) xo[k] = 0.f;
         }
       }
-      const float s = rows_sumsq(w, m, e, xch, XLD);
-      if ((e & 7) == 0 && gr0 + (e >> 3) < P.n_valid) P.ss_out[t * P.ss_stride + gr0 + (e >> 3)] = s;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) xo[k] = gr < P.n_valid ? xo[k] + v[k] : 0.f;
+      const float s = row_sumsq(xo);
+      if (gr < P.n_valid) {
+        const size_t off = static_cast<size_t>(gr) * P.y_ld + t * 128 + c0;
+        st16(P.y + off, xo);
+        if (P.trace) st16(P.trace + off, xo);
+        float w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w[k] = xo[k] * g[k];
+        st16_split(P.yb + static_cast<size_t>(gr) * P.yb_ld + t * 128 + c0, lo_off, w);
+        if ((e & 7) == 0) P.ss_out[t * P.ss_stride + gr] = s;
+      }
     } break;
 
     case OP_SWIGLU: {
-      float val[16];
+      // features 0-63 of the tile are gate rows, 64-127 the matching up rows: lanes 0-3 of a
+      // row group hold gate values, lanes 4-7 the up values they pair with
+      const float inv = s_inv[lr];
+      float a[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        val[j] = v[j] * s_inv[lr0 + j];
-        xch[j * XLD + m] = val[j];
+      for (int k = 0; k < 16; ++k) {
+        const float val = v[k] * inv;
+        const float up = __shfl_xor_sync(0xffffffffu, val, 4, 8);
+        a[k] = val / (1.f + __expf(-val)) * up;
       }
-      named_bar_sync(1, 128);
-      if (m < 64) {
-        const int i = t * 64 + m;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float gt = val[j];
-          const float up = xch[j * XLD + m + 64];
-          const float a = gt / (1.f + __expf(-gt)) * up;
-          if (gr0 + j < P.n_valid) st_split(P.yb + static_cast<size_t>(gr0 + j) * P.yb_ld + i, lo_off, a);
-        }
-      }
-      named_bar_sync(1, 128);
+      if (c0 < 64 && gr < P.n_valid) st16_split(P.yb + static_cast<size_t>(gr) * P.yb_ld + t * 64 + c0, lo_off, a);
     } break;
 
     case OP_LMHEAD: {
-      const int vid = t * 128 + m;
-      const bool vok = vid < P.vocab;
+      const int vid0 = t * 128 + c0;
       const int B = P.rows_per_seq;
+      const float inv = s_inv[lr];
+      float z[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float z = v[j] * s_inv[lr0 + j];
-        const int gr = gr0 + j;
-        if (P.logits && vok && gr < P.n_valid) {
-          const int s = gr / B, i = gr - s * B;
-          if (i >= 1) P.logits[(static_cast<size_t>(s) * (B - 1) + i - 1) * P.vocab + vid] = z;
+      for (int k = 0; k < 16; ++k) z[k] = v[k] * inv;
+      if (P.logits && gr < P.n_valid) {
+        const int sq = gr / B, i = gr - sq * B;
+        if (i >= 1) {
+          float* dst = P.logits + (static_cast<size_t>(sq) * (B - 1) + i - 1) * P.vocab + vid0;
+          if (vid0 + 16 <= P.vocab && (P.vocab & 3) == 0) {
+            st16(dst, z);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              if (vid0 + k < P.vocab) dst[k] = z[k];
+          }
         }
-        xch[j * XLD + m] = vok ? z : -INFINITY;
       }
-      named_bar_sync(1, 128);
-      const int j = e >> 3, part = e & 7;
+      // running argmax of the row, lowest index on ties
       float bv = -INFINITY;
       int bi = 0x7fffffff;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int mm = part * 16 + k;
-        const float z = xch[j * XLD + mm];
-        if (z > bv) { bv = z; bi = t * 128 + mm; }
-      }
+      for (int k = 0; k < 16; ++k)
+        if (vid0 + k < P.vocab && z[k] > bv) {
+          bv = z[k];
+          bi = vid0 + k;
+        }
 #pragma unroll
       for (int off = 4; off >= 1; off >>= 1) {
         const float ov = __shfl_down_sync(0xffffffffu, bv, off, 8);
         const int oi = __shfl_down_sync(0xffffffffu, bi, off, 8);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
-      if (part == 0) {
-        const int lr = lr0 + j;
-        if (bv > s_bv[lr] || (bv == s_bv[lr] && bi < s_bi[lr])) { s_bv[lr] = bv; s_bi[lr] = bi; }
+      if ((e & 7) == 0 && (bv > s_bv[lr] || (bv == s_bv[lr] && bi < s_bi[lr]))) {
+        s_bv[lr] = bv;
+        s_bi[lr] = bi;
       }
-      named_bar_sync(1, 128);
     } break;
   }
 }
@@ -654,29 +722,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       if (u0 < u1) {
         for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
           const int acc = lt & 1;
-          float xpre[16];
-          if (NB == 1 && P.op == OP_RESID) {   // the residual this tile will update, read ahead
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              xpre[j] = (P.grow0 + j < P.n_valid)
-                            ? __ldcg(P.y + static_cast<size_t>(P.grow0 + j) * P.y_ld + t * 128 + m)
-                            : 0.f;
-          }
           EpiPre pre;
-          pre.have = NB == 1;
-          if (NB == 1) {
-            if (P.op == OP_RESID || P.op == OP_FC) {
-              pre.g = bf2f(P.gain[t * 128 + m]);
-            } else if (P.op == OP_KV || P.op == OP_QKV) {
-              const int mi = map_of_tile(P, t);
-              if (P.op == OP_KV ? !(mi & 1) : mi < 2) {
-                int pos[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) pos[j] = max(s_pos[j], 0);
-                rope_tables16(pos, m, P.d, P.rope_cos, P.rope_sin, pre.cs, pre.sn);
-              }
-            }
-          }
+          epilogue_prefetch<NB, C::MINB>(P, t, e, s_pos, pre);
           if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
           named_bar_sync(1, 128);
           if (!s_misc[1 + acc]) {
@@ -690,25 +737,31 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::NCOL;
           if (ca == cb) {
             for (int ch = 0; ch < NB; ++ch) {
-              float v[16];
+              float v[16], w[16];
               tmem_ld_acc(taddr, ch, split, v);
               if (ch == NB - 1) {
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
               }
-              epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq, pre);
+              to_rows<C::XLD>(v, m, e, xch, w);
+              epilogue_rows<NB>(P, t, ch, w, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
           } else {
+            // split tile: every contributor stores its partial ([ROWS][128] fp32, row layout);
+            // the last to arrive sums all of them in CTA order and runs the epilogue
             const int slot = part_slot(c, t, U, Gp, P.KB);
             float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
+            const RowPos rp = row_pos(e);
             for (int ch = 0; ch < NB; ++ch) {
-              float v[16];
+              float v[16], w[16];
               tmem_ld_acc(taddr, ch, split, v);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) dst[(ch * 16 + j) * 128 + m] = v[j];
+              if (ch == NB - 1) {
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+              }
+              to_rows<C::XLD>(v, m, e, xch, w);
+              st16(dst + (ch * 16 + rp.r) * 128 + rp.c0, w);
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
             __threadfence();
             named_bar_sync(1, 128);
             if (e == 0) {
@@ -723,33 +776,25 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               for (int ch = 0; ch < NB; ++ch) {
                 float v[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                // partials summed in CTA order; up to 8 CTAs' loads in flight per round, JC rows
-                // of the chunk at a time (all 16 unless the register budget is halved)
-                constexpr int JC = C::MINB == 1 ? 16 : 4;
-                for (int cc0 = ca; cc0 <= cb; cc0 += 8) {
+                for (int k = 0; k < 16; ++k) v[k] = 0.f;
+                // partials summed in CTA order, up to PR CTAs' loads in flight per round
+                constexpr int PR = C::MINB == 1 ? 8 : 4;
+                for (int cc0 = ca; cc0 <= cb; cc0 += PR) {
+                  float a[PR][16];
 #pragma unroll
-                  for (int h = 0; h < 16 / JC; ++h) {
-                    float a[8][JC];
+                  for (int q2 = 0; q2 < PR; ++q2)
+                    if (cc0 + q2 <= cb)
+                      ld16(P.part + static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                               (ch * 16 + rp.r) * 128 + rp.c0,
+                           a[q2]);
 #pragma unroll
-                    for (int q2 = 0; q2 < 8; ++q2) {
-                      if (cc0 + q2 <= cb) {
-                        const float* src = P.part +
-                                           static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
-                                           (ch * 16 + h * JC) * 128 + m;
+                  for (int q2 = 0; q2 < PR; ++q2)
+                    if (cc0 + q2 <= cb) {
 #pragma unroll
-                        for (int j = 0; j < JC; ++j) a[q2][j] = __ldcg(src + j * 128);
-                      }
+                      for (int k = 0; k < 16; ++k) v[k] += a[q2][k];
                     }
-#pragma unroll
-                    for (int q2 = 0; q2 < 8; ++q2)
-                      if (cc0 + q2 <= cb) {
-#pragma unroll
-                        for (int j = 0; j < JC; ++j) v[h * JC + j] += a[q2][j];
-                      }
-                  }
                 }
-                epilogue_apply<NB, C::XLD>(P, t, ch, v, m, e, xch, s_inv, s_bv, s_bi, xpre, s_pos, s_seq, pre);
+                epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
               }
             }
           }
@@ -845,7 +890,6 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   }
 }
 
-constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA on sm_103
 
 template <class C>
 static int launch_cfg(const GemvChain& p, int n_ctas, cudaStream_t stream, bool pdl) {

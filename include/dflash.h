@@ -155,9 +155,11 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
  * keys, output projection, RMSNorm, SwiGLU MLP (pre-norm, residual adds); then the final
  * RMSNorm, the LM head on slots 1..B-1 and argmax (lowest index on ties).
  *   drafted   int32 [batch][B-1] out: d_1..d_{B-1}
- *   logits    fp32 [batch][B-1][V] out, or NULL (parity checks only; costs bandwidth)
+ *   logits    fp32 [batch][B-1][V] out, or NULL (parity checks only; costs bandwidth);
+ *             16-byte aligned
  *   x_trace   fp32 [L+1][batch*B][H] out, or NULL: block input then the residual after
- *             every layer (parity checks only)
+ *             every layer (parity checks only); 16-byte aligned
+ * A misaligned logits or x_trace returns DFLASH_E_INVAL before any launch.
  * Needs len[s] + B <= kv_capacity (else DFLASH_DEV_CAPACITY and the sequence's cache
  * writes are skipped). len is not changed. */
 int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* drafted,
