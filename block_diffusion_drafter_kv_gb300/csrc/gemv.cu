@@ -746,9 +746,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               to_rows<C::XLD>(v, m, e, xch, w);
               epilogue_rows<NB>(P, t, ch, w, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
-          } else {
-            // split tile: every contributor stores its partial ([ROWS][128] fp32, row layout);
-            // the last to arrive sums all of them in CTA order and runs the epilogue
+          } else if (c != ca) {
+            // split tile, contributor: its partial goes to its slot ([ROWS][128] fp32, row
+            // layout), then it is counted in
             const int slot = part_slot(c, t, U, Gp, P.KB);
             float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
             const RowPos rp = row_pos(e);
@@ -764,38 +764,68 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             }
             __threadfence();
             named_bar_sync(1, 128);
+            if (e == 0) atomicAdd(P.tile_cnt + t, 1);
+          } else {
+            // split tile, finisher: CTA ca, whose last tile this is. The others reach it first
+            // (cb) or only (CTAs in between), so ca is usually the last to get here; it keeps
+            // its own sum, waits for the cb - ca other partials and adds them in CTA order.
+            const RowPos rp = row_pos(e);
+            float own[16];
+            if (NB == 1) {  // own accumulator out of TMEM while the others finish
+              float v[16];
+              tmem_ld_acc(taddr, 0, split, v);
+              tc_fence_before();
+              mbar_arrive(&tempty[acc]);
+              to_rows<C::XLD>(v, m, e, xch, own);
+            }
             if (e == 0) {
-              const int old = atomicAdd(P.tile_cnt + t, 1);
-              const int last = (old == cb - ca);
-              if (last) P.tile_cnt[t] = 0;
-              s_misc[0] = last;
+              const bool ok = grid_wait(P.tile_cnt + t, cb - ca);
+              if (ok) P.tile_cnt[t] = 0;
+              s_misc[0] = ok ? 1 : 0;
             }
             named_bar_sync(1, 128);
-            if (s_misc[0]) {
-              __threadfence();
-              for (int ch = 0; ch < NB; ++ch) {
-                float v[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = 0.f;
-                // partials summed in CTA order, up to PR CTAs' loads in flight per round
-                constexpr int PR = C::MINB == 1 ? 8 : 4;
-                for (int cc0 = ca; cc0 <= cb; cc0 += PR) {
-                  float a[PR][16];
-#pragma unroll
-                  for (int q2 = 0; q2 < PR; ++q2)
-                    if (cc0 + q2 <= cb)
-                      ld16(P.part + static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
-                               (ch * 16 + rp.r) * 128 + rp.c0,
-                           a[q2]);
-#pragma unroll
-                  for (int q2 = 0; q2 < PR; ++q2)
-                    if (cc0 + q2 <= cb) {
-#pragma unroll
-                      for (int k = 0; k < 16; ++k) v[k] += a[q2][k];
-                    }
-                }
-                epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
+            if (!s_misc[0]) {
+              if (e == 0) raise_flag(err, kDevTimeout);
+              if (NB != 1) {
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
               }
+              alive = false;
+              break;
+            }
+            __threadfence();
+            for (int ch = 0; ch < NB; ++ch) {
+              float v[16];
+              if (NB == 1) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = own[k];
+              } else {
+                float a0[16];
+                tmem_ld_acc(taddr, ch, split, a0);
+                if (ch == NB - 1) {
+                  tc_fence_before();
+                  mbar_arrive(&tempty[acc]);
+                }
+                to_rows<C::XLD>(a0, m, e, xch, v);
+              }
+              // the others' partials, up to PR CTAs' loads in flight per round
+              constexpr int PR = C::MINB == 1 ? 8 : 4;
+              for (int cc0 = ca + 1; cc0 <= cb; cc0 += PR) {
+                float a[PR][16];
+#pragma unroll
+                for (int q2 = 0; q2 < PR; ++q2)
+                  if (cc0 + q2 <= cb)
+                    ld16(P.part + static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                             (ch * 16 + rp.r) * 128 + rp.c0,
+                         a[q2]);
+#pragma unroll
+                for (int q2 = 0; q2 < PR; ++q2)
+                  if (cc0 + q2 <= cb) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] += a[q2][k];
+                  }
+              }
+              epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
           }
         }

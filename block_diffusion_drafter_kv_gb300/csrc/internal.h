@@ -12,8 +12,8 @@ namespace dfl {
 // Y = X · Wᵀ over a weight matrix streamed once from HBM: the weight tile (128 output rows
 // x 64 k) is the 128-row A operand of tcgen05.mma, the <= 256 activation rows are the N
 // operand. Work is split "stream-K" style: the (tile, k-block) units are divided evenly
-// over the CTAs; a tile split between CTAs is reduced in a fixed order by whichever CTA
-// finishes it last, so results never depend on timing.
+// over the CTAs; a tile split between CTAs is reduced in a fixed order by the CTA whose
+// last tile it is, once the others' partials are in, so results never depend on timing.
 enum GemvOp : int {
   OP_PLAIN = 0,   // Y fp32
   OP_FC = 1,      // context fusion: cfeat = bf16(F * g_ctx), per-tile sum of squares of F
