@@ -223,6 +223,8 @@ int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pd
 // ---------------------------------------------------------------- synthetic target (harness)
 __global__ void plant_kernel(float* logits, const int* drafted, const uint8_t* masks, int n_steps,
                              const int* step, int batch, int B, int V, float bump, int* saved) {
+  pdl_wait();  // the drafts are final once the previous kernel has completed
+  pdl_launch_dependents();
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= batch * B) return;
   const int s = k / B, i = k - s * B;
@@ -239,22 +241,39 @@ __global__ void plant_kernel(float* logits, const int* drafted, const uint8_t* m
 }
 
 __global__ void unplant_kernel(float* logits, int* step, int n_steps, int batch, int B, const int* saved) {
+  pdl_wait();  // the verification reading these logits has completed
+  pdl_launch_dependents();
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k < batch * B && saved[2 * k] >= 0) logits[saved[2 * k]] = __int_as_float(saved[2 * k + 1]);
   if (k == 0) *step = (*step + 1) % n_steps;
 }
 
+// Both harness kernels are launched with programmatic dependent launch: they can be
+// resident before the previous kernel ends and wait for it in pdl_wait().
+static cudaLaunchConfig_t small_cfg(int n, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 int launch_plant(float* logits, const int* drafted, const uint8_t* masks, int n_steps, const int* step, int batch,
                  int B, int V, float bump, int* saved, cudaStream_t stream) {
-  const int n = batch * B;
-  plant_kernel<<<(n + 255) / 256, 256, 0, stream>>>(logits, drafted, masks, n_steps, step, batch, B, V, bump, saved);
-  return static_cast<int>(cudaGetLastError());
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = small_cfg(batch * B, stream, attr);
+  return static_cast<int>(
+      cudaLaunchKernelEx(&cfg, plant_kernel, logits, drafted, masks, n_steps, step, batch, B, V, bump, saved));
 }
 
 int launch_unplant(float* logits, int* step, int n_steps, int batch, int B, const int* saved, cudaStream_t stream) {
-  const int n = batch * B;
-  unplant_kernel<<<(n + 255) / 256, 256, 0, stream>>>(logits, step, n_steps, batch, B, saved);
-  return static_cast<int>(cudaGetLastError());
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = small_cfg(batch * B, stream, attr);
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, unplant_kernel, logits, step, n_steps, batch, B, saved));
 }
 
 }  // namespace dfl
