@@ -14,6 +14,7 @@ from typing import Optional
 from .build import LIB_PATH
 
 DFLASH_OK = 0
+DFLASH_E_INVAL = -1
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: "capacity exceeded",
           -4: "CUDA error", -5: "state not bound"}
 DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4

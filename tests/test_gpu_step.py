@@ -170,3 +170,27 @@ def _step_loop(tiny, B):
         tiny.oracle.inject(st, bits[:, N:N + tau])
     torch.cuda.synchronize()
     assert int(d.len[0]) == st.length
+
+
+def test_draft_rejects_misaligned_output_buffers(tiny):
+    """logits and x_trace are written 16 bytes at a time: a buffer that is not 16-byte
+    aligned is refused before any launch, and the handle stays usable."""
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    s, d = tiny.s, tiny.drafter
+    B = 4
+    drafted = torch.zeros(1, B - 1, dtype=torch.int32, device="cuda")
+    flat = torch.zeros((B - 1) * s.vocab + 1, device="cuda")
+    with pytest.raises(BND.DFlashError) as ei:
+        d.draft(1, B, drafted, flat[1:].view(1, B - 1, s.vocab))
+    assert ei.value.status == BND.DFLASH_E_INVAL
+    trace = torch.zeros((s.n_layers + 1) * B * s.hidden + 1, device="cuda")
+    with pytest.raises(BND.DFlashError) as ei:
+        d.draft(1, B, drafted, None, trace[1:])
+    assert ei.value.status == BND.DFLASH_E_INVAL
+    d.device_error()  # clear what earlier tests left
+    d.len.zero_()
+    d.last_token.zero_()
+    d.draft(1, B, drafted, flat[: (B - 1) * s.vocab].view(1, B - 1, s.vocab))
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    assert bool(torch.isfinite(flat[: (B - 1) * s.vocab]).all())
