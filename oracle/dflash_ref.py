@@ -217,8 +217,7 @@ class Oracle:
         H, nq, nkv, d = s.hidden, s.n_heads, s.n_kv_heads, s.head_dim
         N = st.length
         x = np.empty((B, H), dtype=self.dtype)
-        x[0] = self.W("embed")[st.last_token] if self._cache is not None else \
-            bf16_to_float(self.bits["embed"][st.last_token], self.dtype)
+        x[0] = self._embed_row(st.last_token)
         x[1:] = self.W("mask_emb")
         trace = [x.copy()]
         pos = np.arange(N, N + B)
@@ -246,6 +245,13 @@ class Oracle:
         else:                                                            # no drafted slots
             gap = np.zeros(0, dtype=self.dtype)
         return DraftResult(drafted.astype(np.int64), logits, np.stack(trace), gap)
+
+    def _embed_row(self, tok: int) -> np.ndarray:
+        """Row `tok` of the token embedding E (slot 0 of the block). Without the widened-weight
+        cache only that one row of E is widened."""
+        if self._cache is not None:
+            return self.W("embed")[tok]
+        return bf16_to_float(self.bits["embed"][tok], self.dtype)
 
     def _lm_head(self, h: np.ndarray) -> np.ndarray:
         V = self.s.vocab

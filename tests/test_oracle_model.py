@@ -109,3 +109,65 @@ def test_fp32_mode_close_to_fp64(tiny):
         r[dt] = o.draft(st, 4)
     a, b = r[np.float64], r[np.float32]
     assert np.max(np.abs(a.logits - b.logits)) < 1e-4 * np.std(a.logits) * 100
+
+
+def _uncached(s, bits):
+    """The oracle as the full-size workloads run it: weights widened per use (no cache, the
+    branch taken once the widened weights exceed the cache limit) and the LM head in row
+    chunks, here of an odd size (7) that divides no dimension of the tiny drafter."""
+    o = Oracle(s, bits, cache_limit_bytes=0, lm_chunk=7)
+    assert o._cache is None
+    return o
+
+
+def test_uncached_chunked_oracle_matches_naive(tiny):
+    """The uncached, chunked branch against the naive per-slot recomputation, over three
+    draft+verify steps with incremental injection (as the cached branch is pinned above)."""
+    s, bits, hid = tiny
+    w = W_TINY
+    o = _uncached(s, bits)
+    last = int(I.initial_tokens(1, s.vocab, SEED + 1)[0])
+    st = o.new_sequence(w.kv_capacity(), last)
+    o.inject(st, hid[:, : w.ctx])
+    K, V = naive_context_kv(s, bits, hid[:, : w.ctx])
+    for l in range(s.n_layers):
+        assert np.allclose(st.k_cache[l][: w.ctx], K[l], atol=1e-10)
+        assert np.allclose(st.v_cache[l][: w.ctx], V[l], atol=1e-10)
+    for step in range(w.steps):
+        r = o.draft(st, w.block)
+        nd, nl, ntr = naive_draft(s, bits, hid[:, : st.length], st.last_token, w.block)
+        assert np.array_equal(r.drafted, nd)
+        assert np.allclose(r.logits, nl, rtol=1e-9, atol=1e-10)
+        assert np.allclose(r.x_trace, ntr, rtol=1e-9, atol=1e-10)
+        noise = I.make_logit_noise(1, w.block, s.vocab, SEED + 1, f"logits.{step}").numpy()
+        mask = I.make_plant_mask(1, w.block, w.p_plant, SEED + 1, f"plant.{step}")
+        v = o.verify(st, I.plant_logits(noise, r.drafted[None], mask)[0], r.drafted)
+        o.inject(st, hid[:, st.length: st.length + v.accept_len])
+
+
+def test_uncached_chunked_oracle_equals_cached(tiny):
+    """Both branches compute the same step: inject, draft and verify agree to fp64 rounding
+    over three steps (the chunked LM head computes each logit as one whole dot product)."""
+    s, bits, hid = tiny
+    w = W_TINY
+    a, b = Oracle(s, bits), _uncached(s, bits)
+    assert a._cache is not None
+    last = int(I.initial_tokens(1, s.vocab, SEED + 2)[0])
+    sa, sb = a.new_sequence(w.kv_capacity(), last), b.new_sequence(w.kv_capacity(), last)
+    a.inject(sa, hid[:, : w.ctx])
+    b.inject(sb, hid[:, : w.ctx])
+    for step in range(w.steps):
+        ra, rb = a.draft(sa, w.block), b.draft(sb, w.block)
+        assert np.array_equal(ra.drafted, rb.drafted)
+        assert np.allclose(ra.logits, rb.logits, rtol=1e-12, atol=1e-13)
+        assert np.allclose(ra.x_trace, rb.x_trace, rtol=1e-12, atol=1e-13)
+        noise = I.make_logit_noise(1, w.block, s.vocab, SEED + 2, f"logits.{step}").numpy()
+        mask = I.make_plant_mask(1, w.block, w.p_plant, SEED + 2, f"plant.{step}")
+        T = I.plant_logits(noise, ra.drafted[None], mask)[0]
+        va, vb = a.verify(sa, T, ra.drafted), b.verify(sb, T, rb.drafted)
+        assert va.accept_len == vb.accept_len and np.array_equal(va.committed, vb.committed)
+        a.inject(sa, hid[:, sa.length: sa.length + va.accept_len])
+        b.inject(sb, hid[:, sb.length: sb.length + vb.accept_len])
+        for l in range(s.n_layers):
+            assert np.allclose(sa.k_cache[l][: sa.length], sb.k_cache[l][: sb.length], rtol=1e-12, atol=1e-13)
+            assert np.allclose(sa.v_cache[l][: sa.length], sb.v_cache[l][: sb.length], rtol=1e-12, atol=1e-13)

@@ -121,6 +121,24 @@ def _ctx_no_norm(self, hidden_bits):
     return (X @ self.W("w_fc").T) * self.W("g_ctx")
 
 
+def _lm_chunk_short(self, h):   # each chunk one LM-head row short of its bound
+    V = self.s.vocab
+    if self._cache is not None:
+        return h @ self.W("lm_head").T
+    out = np.zeros((h.shape[0], V), dtype=self.dtype)
+    bits = self.bits["lm_head"]
+    for v0 in range(0, V, self.lm_chunk):
+        v1 = min(V, v0 + self.lm_chunk - 1)
+        out[:, v0:v1] = h @ R.bf16_to_float(bits[v0:v1], self.dtype).T
+    return out
+
+
+def _embed_row_next(self, tok):   # the uncached lookup widens the row after the token's
+    if self._cache is not None:
+        return self.W("embed")[tok]
+    return R.bf16_to_float(self.bits["embed"][(tok + 1) % self.s.vocab], self.dtype)
+
+
 MUTATIONS = {
     "rope_sign": ("apply_rope", _rope_wrong_sign),
     "rope_interleaved_pairs": ("apply_rope", _rope_interleaved),
@@ -136,6 +154,8 @@ MUTATIONS = {
     "verify_skips_mismatch": ("verify_greedy", _verify_skip_mismatch),
     "fc_taps_reversed": ("Oracle.context_feature", _ctx_taps_reversed),
     "fc_missing_rmsnorm": ("Oracle.context_feature", _ctx_no_norm),
+    "lm_chunk_bound_short": ("Oracle._lm_head", _lm_chunk_short),
+    "uncached_embed_wrong_row": ("Oracle._embed_row", _embed_row_next),
 }
 
 
@@ -156,6 +176,8 @@ def _all_pins(tiny):
         "verify_lossless": V.test_lossless_committed_equal_target_greedy,
         "inject_naive": lambda: MM.test_injection_matches_naive(tiny),
         "draft_naive": lambda: MM.test_draft_steps_match_naive_recomputation(tiny),
+        "uncached_naive": lambda: MM.test_uncached_chunked_oracle_matches_naive(tiny),
+        "uncached_equals_cached": lambda: MM.test_uncached_chunked_oracle_equals_cached(tiny),
     }
     for name, fn in checks.items():
         try:
