@@ -65,9 +65,10 @@ def peaks():
 def proj_bytes_flops(s, batch, B, tau):
     """Algorithmic (bytes, flops) of each projection: the weight read once, the activation
     rows read once, the outputs written once. bf16 activation operands are two planes
-    (high and low, 4 bytes per value); q and the K cache are fp32, the V cache bf16; the
-    residual stream is fp32 (read and written by O and down). FLOPs count one product per
-    weight and row (the low plane's second product is not counted)."""
+    (high and low, 4 bytes per value); q is fp32; K and V cache entries count 2 bytes each
+    (bf16, the method's KV; the library's fp32 K storage is excess traffic, reported
+    apart); the residual stream is fp32 (read and written by O and down). FLOPs count one
+    product per weight and row (the low plane's second product is not counted)."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     rows = batch * B
     kin = s.n_taps * s.target_hidden
@@ -77,8 +78,8 @@ def proj_bytes_flops(s, batch, B, tau):
     nqd = s.n_heads * d
     return {
         "fc": (2 * H * kin + 2 * tau * kin + 4 * tau * H, 2 * tau * H * kin),
-        "kv": (2 * kv * H + 4 * tau * H + 3 * tau * kv, 2 * tau * kv * H),
-        "qkv": (2 * nqkv * H + 4 * rows * H + rows * (4 * nqd + 6 * kvd), 2 * rows * nqkv * H),
+        "kv": (2 * kv * H + 4 * tau * H + 2 * tau * kv, 2 * tau * kv * H),
+        "qkv": (2 * nqkv * H + 4 * rows * H + rows * (4 * nqd + 4 * kvd), 2 * rows * nqkv * H),
         "o": (2 * H * nqd + 4 * rows * nqd + 12 * rows * H, 2 * rows * H * nqd),
         "gateup": (2 * 2 * I * H + 4 * rows * (H + I), 2 * rows * 2 * I * H),
         "down": (2 * H * I + 4 * rows * I + 12 * rows * H, 2 * rows * H * I),
@@ -87,9 +88,9 @@ def proj_bytes_flops(s, batch, B, tau):
 
 
 def attn_bytes_flops(s, batch, B, n_ctx):
-    """K (fp32) and V (bf16) read once per layer per sequence (context plus block keys),
-    q (fp32) read, o (two bf16 planes) written."""
-    kvb = 6 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
+    """K and V read once per layer per sequence (context plus block keys) at 2 bytes per
+    element each (bf16, the method's KV), q (fp32) read, o (two bf16 planes) written."""
+    kvb = 4 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
     qo = 8 * batch * B * s.n_heads * s.head_dim
     fl = 4 * batch * B * s.n_heads * s.head_dim * (n_ctx + B)
     return kvb + qo, fl
@@ -99,13 +100,13 @@ def _passes(rows, width):
     return [(r0, min(width, rows - r0)) for r0 in range(0, rows, width)]
 
 
-def launch_plan(s, batch, B, tau, n_ctx, n_sms=152, one_pass=False):
+def launch_plan(s, batch, B, tau, n_ctx, n_sms=152, one_pass=False, chain_max=8):
     """Launch order of one step by call: (label, kind, bytes, flops). kind "gemv" marks the
-    chained kernel (one launch runs up to DFLASH_CHAIN_MAX phases, for one pass of at most
-    128 rows); attention is a launch of its own between chains. Injection runs in passes of
-    a width fixed by max_batch * max_block. Mirrors the library's grouping. With one_pass
-    every projection covers all rows at once: the method's own traffic, each weight once."""
-    chain_max = int(os.environ.get("DFLASH_CHAIN_MAX", "8"))
+    chained kernel (one launch runs up to `chain_max` phases, the handle's
+    DFLASH_OPT_CHAIN_MAX, for one pass of at most 128 rows); attention is a launch of its own
+    between chains. Injection runs in passes of a width fixed by max_batch * max_block.
+    Mirrors the library's grouping. With one_pass every projection covers all rows at once:
+    the method's own traffic, each weight once."""
     ab = attn_bytes_flops(s, batch, B, n_ctx)
     rows = batch * B
     nb = 1
@@ -152,6 +153,16 @@ def measured_traffic(launch, workload):
     return t["traffic_bytes"] if h.hexdigest() == t["sources_sha256"] else None
 
 
+def kv_storage_excess(s, batch, B, n_ctx, tau):
+    """Bytes per step the library moves beyond the method's bf16 K/V because it stores K
+    as fp32 (TF32-rounded): 2 more bytes per K element read by attention in every layer,
+    and per K element written by injection and by the block's Q/K/V projection."""
+    kvd = s.n_kv_heads * s.head_dim
+    read = 2 * (n_ctx + B) * kvd * batch * s.n_layers
+    written = 2 * (tau + B) * kvd * batch * s.n_layers
+    return read + written
+
+
 def step_bytes_flops(s, batch, B, n_ctx, tau):
     """Algorithmic bytes and FLOPs of one step: every weight read once, K/V read once per
     layer, activations and logits once (however the library splits rows into passes)."""
@@ -164,6 +175,76 @@ def step_bytes_flops(s, batch, B, n_ctx, tau):
 
 
 # ------------------------------------------------------------------ clocks
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, read through NVML
+    (the driver's management library, loaded with ctypes) every `period_ms` from a thread.
+    Only reads; changes no setting. Raises in __init__ when NVML is not usable."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, pci_bus_id: str, period_ms=1.0):
+        import ctypes
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + pci_bus_id)
+        try:
+            self._reasons = self.nv.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.period = period_ms / 1e3
+        self.samples = []
+        self._stop = False
+        self._t = None
+
+    def _read_one(self):
+        import ctypes
+        clk, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self._reasons(self.h, ctypes.byref(rs))
+        return float(clk.value), pw.value / 1e3, int(rs.value)
+
+    def _loop(self):
+        while not self._stop:
+            self.samples.append((time.monotonic(), *self._read_one()))
+            time.sleep(self.period)
+
+    def start(self):
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        self._stop = True
+        if self._t:
+            self._t.join(timeout=2)
+
+    def summary(self, t0, t1, gpu_index=None):
+        inside = [r for r in self.samples if t0 <= r[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "no NVML sample inside the timed region"}
+        reasons = sorted({n for r in inside for bit, n in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(r[2] for r in inside), "reasons": reasons, "samples": len(inside),
+                "note": "NVML, sampled every ~1 ms during the timed region"}
+
+
+def clock_sampler():
+    """NVML sampler for the current CUDA device, else the nvidia-smi one."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        return NvmlClockSampler(bus)
+    except Exception:
+        return ClockSampler()
+
 
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -276,6 +357,21 @@ def job_rate(ws: int, batch: int, steps: int, seconds: float) -> float:
     return ws * batch * steps / seconds
 
 
+def workload_config(w, ws, seed):
+    """The `config` object of the JSON line, the same for both arms: what the workload is."""
+    from synth import weight_bytes
+    from synth import inputs as I
+    s = w.shape
+    wb = weight_bytes(s)
+    return {"workload": w.name, "batch_per_gpu": w.batch, "block": w.block,
+            "ctx": int(I.ragged_ctx(w, seed).mean()),
+            "drafter": f"H{s.hidden} L{s.n_layers} nq{s.n_heads} nkv{s.n_kv_heads} d{s.head_dim} "
+                       f"I{s.intermediate} V{s.vocab} k{s.n_taps}",
+            "p_plant": w.p_plant, "parallelism": f"replicas x{ws}",
+            "l2": f"inputs larger than L2: {sum(v for k, v in wb.items() if k != 'embed_row') / 1e9:.2f} "
+                  "GB of weights streamed per step, no flush"}
+
+
 def run_reference(a):
     ws, rank, _ = dist_info()
     if rank != 0:
@@ -291,20 +387,22 @@ def run_reference(a):
     step_bits = I.bf16_bits(I.make_hidden(s, w.block, a.seed, "step"))
     noise = I.make_logit_noise(1, w.block, s.vocab, a.seed).numpy()[0][None]
     masks = [I.make_plant_mask(1, w.block, w.p_plant, a.seed, f"plant.{i}")[0] for i in range(8)]
-    budget = 150.0
+    # W untimed steps, then exactly K timed steps; each step one sequence of the workload
+    # (for the batch-1 workloads, the whole step)
     if a.warmup > 0:
-        oracle_steps(s, bits, w, a.seed, 1, budget, ctx_bits, step_bits, noise[0], masks)
-    n, secs = oracle_steps(s, bits, w, a.seed, a.steps, budget, ctx_bits, step_bits, noise[0], masks)
+        oracle_steps(s, bits, w, a.seed, a.warmup, float("inf"), ctx_bits, step_bits, noise[0], masks)
+    n, secs = oracle_steps(s, bits, w, a.seed, a.steps, float("inf"), ctx_bits, step_bits, noise[0], masks)
     v = n / secs
     cores = cpu_cores()
-    sample = (f"{n} of the requested {a.steps} oracle steps of the {w.name} workload (inject + B={w.block} draft "
-              f"+ verify, fp64 NumPy, one sequence) after an untimed prefill of {w.ctx} positions; "
-              f"warm-up capped at 1 step, time budget {budget:.0f} s")
+    sample = (f"{n} oracle steps of the {w.name} workload (inject + B={w.block} draft + verify, fp64 NumPy, "
+              f"one sequence of {w.batch}) after an untimed prefill of {w.ctx} positions and {a.warmup} "
+              f"untimed warm-up steps")
+    ws, _, _ = dist_info()
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": a.gpus, "steps": n,
-        "warmup": min(a.warmup, 1), "ms_per_step": 1e3 * secs / n, "higher_is_better": True, "scaling": "weak",
+        "warmup": a.warmup, "ms_per_step": 1e3 * secs / n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "batch": 1, "block": w.block, "ctx": w.ctx},
+        "config": workload_config(w, ws, a.seed),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -317,7 +415,7 @@ def run_cuda(a):
 
     from block_diffusion_drafter_kv_gb300 import binding as BND
     from block_diffusion_drafter_kv_gb300.build import build
-    from synth import WORKLOADS, weight_bytes
+    from synth import WORKLOADS
     from synth import inputs as I
 
     ws, rank, local = dist_info()
@@ -394,7 +492,7 @@ def run_cuda(a):
         inject_draft()
         plant_verify()
     stream.synchronize()
-    assert dr.device_error() == 0, "device error flag after the eager step"
+    assert dr.device_error(stream=stream) == 0, "device error flag after the eager step"
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         inject_draft()
@@ -405,7 +503,7 @@ def run_cuda(a):
     stream.synchronize()
 
     # ---------------------------------------------------------------- timed region
-    clocks = ClockSampler()
+    clocks = clock_sampler()
     clocks.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
@@ -432,7 +530,7 @@ def run_cuda(a):
     ms_total = e0.elapsed_time(e1)
     time.sleep(0.1)
     clocks.stop()
-    err = dr.device_error()
+    err = dr.device_error(stream=stream)
     len_end = int(dr.len[:batch].sum())
     tau_sum = (len_end - len_start) + int(accept[:batch].sum())
     mean_tau = tau_sum / (a.steps * batch)
@@ -473,6 +571,29 @@ def run_cuda(a):
     torch.cuda.synchronize()
     draft_ms = d0.elapsed_time(d1) / n_draft
     log(f"[bench] draft alone: {draft_ms * 1e3:.1f} us")
+    # the same for every block size of the sweep (the block rides in the N operand of every
+    # weight stream, so the draft's cost should barely depend on it)
+    draft_by_block = {}
+    for Bs in (4, 8, 12, 16):
+        if Bs > B:
+            continue
+        if Bs == B:
+            draft_by_block[str(Bs)] = draft_ms
+            continue
+        gB = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gB, stream=stream):
+            dr.draft(batch, Bs, drafted)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gB.replay()
+            d0.record(stream)
+            for _ in range(n_draft):
+                gB.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        draft_by_block[str(Bs)] = d0.elapsed_time(d1) / n_draft
+        del gB
+    log("[bench] draft by block: " + json.dumps({k: round(v * 1e3, 1) for k, v in draft_by_block.items()}))
 
     # ---------------------------------------------------------------- traced pass (per-kernel)
     kern = {}
@@ -483,7 +604,7 @@ def run_cuda(a):
             ev.record(stream)
         stream.synchronize()
         dr.trace_events(evs)
-        plan = launch_plan(s, batch, B, tau_avg, n_avg)
+        plan = launch_plan(s, batch, B, tau_avg, n_avg, chain_max=dr.get_option(BND.OPT_CHAIN_MAX))
         with torch.cuda.stream(stream):
             reset()
         stream.synchronize()
@@ -617,20 +738,16 @@ def run_cuda(a):
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
     clk = clocks.summary(th0, th1, gpu_index if gpu_index.isdigit() else None)
     if rank == 0:
-        wb = weight_bytes(s)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden states and logits)",
-            "config": {"workload": w.name, "batch_per_gpu": batch, "block": B, "ctx": int(ctx_lens.mean()),
-                       "drafter": f"H{s.hidden} L{s.n_layers} nq{s.n_heads} nkv{s.n_kv_heads} d{s.head_dim} "
-                                  f"I{s.intermediate} V{s.vocab} k{s.n_taps}",
-                       "p_plant": w.p_plant, "parallelism": f"replicas x{ws}",
-                       "l2": f"inputs larger than L2: {sum(v for k, v in wb.items() if k != 'embed_row') / 1e9:.2f} "
-                             "GB of weights streamed per step, no flush",
-                       "launch": "one CUDA graph per step, programmatic dependent launch between kernels"},
+            "config": workload_config(w, ws, a.seed),
+            "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
             "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
-            "draft_ms": draft_ms,
+            "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block,
+            "draft_flatness": (max(draft_by_block.values()) / min(draft_by_block.values())) if draft_by_block else None,
+            "kv_storage_excess_bytes_per_step": kv_storage_excess(s, batch, B, n_avg, tau_avg),
             "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,
             "clocks": clk, "device_error": err,

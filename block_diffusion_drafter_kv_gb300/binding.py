@@ -18,6 +18,7 @@ DFLASH_E_INVAL = -1
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: "capacity exceeded",
           -4: "CUDA error", -5: "state not bound"}
 DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4
+OPT_WAIT_LIMIT_NS, OPT_CHAIN_MAX, OPT_GEMV_VARIANT, OPT_ATTN_SPLIT = 1, 2, 3, 4
 
 
 class DflashConfig(ctypes.Structure):
@@ -49,7 +50,10 @@ SIGNATURES = {
                                        c_void_p]),
     "dflash_linear_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                      c_void_p]),
-    "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32]),
+    "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32, c_void_p]),
+    "dflash_set_option": (c_int32, [c_void_p, c_int32, ctypes.c_int64]),
+    "dflash_get_option": (c_int32, [c_void_p, c_int32, POINTER(ctypes.c_int64)]),
+    "dflash_selftest_timeout": (c_int32, [c_void_p, c_void_p]),
     "dflash_last_launch_count": (c_int32, [c_void_p]),
     "dflash_trace_events": (c_int32, [c_void_p, POINTER(c_void_p), c_int32]),
     "dflash_timeline": (c_int32, [c_void_p, c_void_p, ctypes.c_int64]),
@@ -169,10 +173,24 @@ class Drafter:
         check(self.L.dflash_linear_bf16(self.h, W.data_ptr(), W.shape[0], W.shape[1], X.data_ptr(), X.shape[0],
                                         Y.data_ptr(), _stream(stream)), "dflash_linear_bf16")
 
-    def device_error(self, clear: bool = True) -> int:
+    def device_error(self, clear: bool = True, stream=None) -> int:
+        """The device error flag once the work queued on `stream` (default: the current
+        stream) has finished; with `clear`, the flag and the kernels' counters are reset."""
         f = c_int32(0)
-        check(self.L.dflash_read_device_error(self.h, ctypes.byref(f), 1 if clear else 0), "dflash_read_device_error")
+        check(self.L.dflash_read_device_error(self.h, ctypes.byref(f), 1 if clear else 0, _stream(stream)),
+              "dflash_read_device_error")
         return f.value
+
+    def set_option(self, option: int, value: int) -> None:
+        check(self.L.dflash_set_option(self.h, option, int(value)), "dflash_set_option")
+
+    def get_option(self, option: int) -> int:
+        v = ctypes.c_int64(0)
+        check(self.L.dflash_get_option(self.h, option, ctypes.byref(v)), "dflash_get_option")
+        return v.value
+
+    def selftest_timeout(self, stream=None) -> None:
+        check(self.L.dflash_selftest_timeout(self.h, _stream(stream)), "dflash_selftest_timeout")
 
     def last_launch_count(self) -> int:
         return self.L.dflash_last_launch_count(self.h)
@@ -204,9 +222,22 @@ class Drafter:
             pass
 
 
+def _require(t, dtype, name):
+    import torch
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise DFlashError(DFLASH_E_INVAL, f"{name} must be a contiguous {dtype} CUDA tensor "
+                                          f"(got {t.dtype}, cuda={t.is_cuda}, contiguous={t.is_contiguous()})")
+
+
 def verify_greedy_noalloc(target_logits, drafted, batch: int, block: int, accept_len, committed, last_token,
                           stream=None):
     """Greedy verification with no handle and no allocation (scratch is a fixed array in the library)."""
+    import torch
+    _require(target_logits, torch.float32, "target_logits")
+    for t, n in ((accept_len, "accept_len"), (committed, "committed"), (last_token, "last_token")):
+        _require(t, torch.int32, n)
+    if drafted is not None:
+        _require(drafted, torch.int32, "drafted")
     check(lib().dflash_verify_greedy_noalloc(target_logits.data_ptr(), _ptr(drafted), batch, block,
                                              target_logits.shape[-1], accept_len.data_ptr(), committed.data_ptr(),
                                              last_token.data_ptr(), _stream(stream)), "dflash_verify_greedy_noalloc")

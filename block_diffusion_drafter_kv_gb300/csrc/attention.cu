@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
 
   for (int i = 0; i < n; ++i) {
     const int st = i % STAGES;
-    if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1)) {
+    if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1, P.wait_ns)) {
       s_flag[0] = 1;
       raise_flag(P.err, kDevTimeout);
     }
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (threadIdx.x == 0 && i + STAGES < n) {
-      if (!s_flag[0] && !mbar_wait(&empty[st], (i / STAGES) & 1)) {
+      if (!s_flag[0] && !mbar_wait(&empty[st], (i / STAGES) & 1, P.wait_ns)) {
         s_flag[0] = 1;
         raise_flag(P.err, kDevTimeout);
       }
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   // merge the rows [rank*per, rank*per + nrow): block c of s_recv came from CTA c
   if (nrow > 0) {
     if (threadIdx.x == 0) {
-      const bool ok = mbar_wait(recv_bar, 0);
+      const bool ok = mbar_wait(recv_bar, 0, P.wait_ns);
       if (!ok) raise_flag(P.err, kDevTimeout);
       s_flag[1] = ok ? 1 : 0;
     }

@@ -149,6 +149,7 @@ int nb_for_rows(int rows) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 }  // namespace
 
@@ -166,6 +167,7 @@ struct dflash_handle {
   int chain_slot = 0;
   int chain_max = kMaxPhases;  // projections per persistent launch (1 = one launch per projection)
   int attn_split = 0;          // CTAs per attention cluster (0: from the SM count)
+  unsigned long long wait_ns = kDefaultWaitLimitNs;  // limit of every wait inside a kernel
   int attn_wide = 0;           // clusters of 12 the device holds at once (0: none)
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
@@ -259,6 +261,7 @@ int run_chain_one(dflash_handle* h, const GemvParams* phases, int n, int nb, cud
   const int G = std::min(h->n_sms, kMaxCtas);
   C.tl = tl_take(h, G);
   C.tl_id = h->tl_launch++;
+  C.wait_ns = h->wait_ns;
   const int e = launch_gemv(C, v, G, st, h->trace_ev.empty());
   note_launch(h, st);
   return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
@@ -311,9 +314,6 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
   h->inject_pass_rows = 16 * nb_for_rows(std::min(cfg->max_batch * cfg->max_block, kMaxPassRows));
-  if (const char* ev = std::getenv("DFLASH_GEMV_VARIANT")) h->gemv_pref = std::atoi(ev);
-  if (const char* ev = std::getenv("DFLASH_ATTN_SPLIT")) h->attn_split = std::max(0, std::min(16, std::atoi(ev)));
-  if (const char* ev = std::getenv("DFLASH_CHAIN_MAX")) h->chain_max = std::max(1, std::min(kMaxPhases, std::atoi(ev)));
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
       gemv_set_attributes() != 0 || attn_set_attributes() != 0) {
@@ -669,6 +669,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     if (h->attn_split > 0) split = h->attn_split;
     A.tl = tl_take(h, static_cast<long long>(split) * c.n_kv_heads * batch);
     A.tl_id = h->tl_launch++;
+    A.wait_ns = h->wait_ns;
     if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
     note_launch(h, st);
     return DFLASH_OK;
@@ -700,6 +701,9 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   if (!h->bound) return DFLASH_E_STATE;
   const auto& c = h->cfg;
   if (!target_logits || !accept_len || !committed || batch < 1 || block < 1 || (block > 1 && !drafted))
+    return DFLASH_E_INVAL;
+  // the logits are read 16 bytes at a time, the token arrays as 4-byte words
+  if (!aligned16(target_logits) || !aligned4(drafted) || !aligned4(accept_len) || !aligned4(committed))
     return DFLASH_E_INVAL;
   if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -762,13 +766,103 @@ int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K
   return DFLASH_OK;
 }
 
-int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear) {
+int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, void* stream) {
   if (!h || !flags) return DFLASH_E_INVAL;
   if (!h->bound) return DFLASH_E_STATE;
-  if (cudaDeviceSynchronize() != cudaSuccess) return DFLASH_E_CUDA;
-  if (cudaMemcpy(flags, h->ws + h->L.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_E_CUDA;
-  if (clear && cudaMemset(h->ws + h->L.err, 0, 4) != cudaSuccess) return DFLASH_E_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, h->ws + h->L.err, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DFLASH_E_CUDA;
+  *flags = v;
+  if (clear) {
+    // The flag, and every arrival counter a kernel that gave up a wait may have left
+    // non-zero (split-tile and phase counters, per-sequence verification counters).
+    const WsLayout& L = h->L;
+    const size_t spans[][2] = {{L.err, 4},
+                               {L.tile_cnt, static_cast<size_t>(L.max_tiles) * 4},
+                               {L.cta_cnt, 4},
+                               {L.seq_cnt, static_cast<size_t>(h->cfg.max_batch) * 4},
+                               {L.chain_bar, static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4}};
+    for (const auto& sp : spans)
+      if (cudaMemsetAsync(h->ws + sp[0], 0, sp[1], st) != cudaSuccess) return DFLASH_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DFLASH_E_CUDA;
+  }
   return DFLASH_OK;
+}
+
+int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
+  if (!h) return DFLASH_E_INVAL;
+  switch (option) {
+    case DFLASH_OPT_WAIT_LIMIT_NS:
+      if (value < 100000 || value > 60000000000LL) return DFLASH_E_INVAL;
+      h->wait_ns = static_cast<unsigned long long>(value);
+      return DFLASH_OK;
+    case DFLASH_OPT_CHAIN_MAX:
+      if (value < 1 || value > kMaxPhases) return DFLASH_E_INVAL;
+      h->chain_max = static_cast<int>(value);
+      return DFLASH_OK;
+    case DFLASH_OPT_GEMV_VARIANT:
+      if (value < 0 || value > 5) return DFLASH_E_INVAL;
+      h->gemv_pref = static_cast<int>(value);
+      return DFLASH_OK;
+    case DFLASH_OPT_ATTN_SPLIT:
+      if (value < 0 || value > 16) return DFLASH_E_INVAL;
+      h->attn_split = static_cast<int>(value);
+      return DFLASH_OK;
+  }
+  return DFLASH_E_INVAL;
+}
+
+int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value) {
+  if (!h || !value) return DFLASH_E_INVAL;
+  switch (option) {
+    case DFLASH_OPT_WAIT_LIMIT_NS: *value = static_cast<int64_t>(h->wait_ns); return DFLASH_OK;
+    case DFLASH_OPT_CHAIN_MAX: *value = h->chain_max; return DFLASH_OK;
+    case DFLASH_OPT_GEMV_VARIANT: *value = h->gemv_pref; return DFLASH_OK;
+    case DFLASH_OPT_ATTN_SPLIT: *value = h->attn_split; return DFLASH_OK;
+  }
+  return DFLASH_E_INVAL;
+}
+
+int dflash_selftest_timeout(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  call_begin(h, st);
+  // Two plain projections of the residual scratch through the output projection of layer
+  // 0 (Y = xg · Woᵀ into the residual scratch, which the next draft rewrites before use).
+  // Phase 1 waits for a barrier count one above the grid size, which no CTA reaches.
+  GemvParams P{};
+  gemv_common(h, P);
+  P.amap[0] = h->m_wo[0];
+  P.n_amaps = 1;
+  P.T = c.hidden / 128;
+  P.tile_start[1] = P.T;
+  P.KB = c.n_heads * c.head_dim / 64;
+  P.bmap = h->m_o[0];
+  P.op = OP_PLAIN;
+  P.n_valid = 16;
+  P.n_out = c.hidden;
+  P.y = h->at<float>(h->L.x);
+  P.y_ld = c.hidden;
+  GemvChain C{};
+  const int v = gemv_variant(1, h->gemv_pref);
+  const int ks = gemv_variant_ksub(v);
+  if (P.KB % ks) return DFLASH_E_CONFIG;
+  C.ph[0] = P;
+  C.ph[0].KB /= ks;
+  C.ph[1] = C.ph[0];
+  C.n_phases = 2;
+  C.bar = h->at<int>(h->L.chain_bar) + h->chain_slot * (kMaxPhases + 4);
+  h->chain_slot = (h->chain_slot + 1) % kChainSlots;
+  C.exit_cnt = C.bar + kMaxPhases;
+  C.wait_ns = h->wait_ns;
+  C.bar_extra = 1;
+  const int e = launch_gemv(C, v, std::min(h->n_sms, kMaxCtas), st, false);
+  note_launch(h, st);
+  return e == 0 ? DFLASH_OK : DFLASH_E_CUDA;
 }
 
 int32_t dflash_last_launch_count(const dflash_handle* h) { return h ? h->last_launches : 0; }

@@ -52,7 +52,7 @@ struct GemvCfg {
   static constexpr int TMEM_COLS = 2 * NCOL;          // two accumulators (power of two >= 64)
   static constexpr int XLD = 132;                     // padded row of the exchange buffer
   static constexpr int EPI_BYTES = 16 * XLD * 4 + 5 * ROWS * 4;  // xch, inv, best v/i, row pos/seq
-  static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 32;
+  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC2 = idesc_bf16_f32(128, NCOL);  // high and low planes
   static constexpr uint32_t IDESC1 = idesc_bf16_f32(128, ROWS);  // high plane only
@@ -435,19 +435,19 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
 }
 
 // Grid-wide phase barrier: every CTA arrives once per phase after its epilogue work is
-// done; a waiter sees all of that phase's stores. Bounded: false after kWaitLimitNs.
+// done; a waiter sees all of that phase's stores. Bounded: false after limit_ns.
 DEV int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-DEV bool grid_wait(const int* bar, int target) {
+DEV bool grid_wait(const int* bar, int target, uint64_t limit_ns) {
   if (ld_acquire_gpu(bar) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     __nanosleep(64);
     if (ld_acquire_gpu(bar) >= target) return true;
-    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 // Order this thread's generic-proxy global stores before later async-proxy (TMA) reads.
@@ -487,12 +487,14 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* mdone = tempty + 2;  // completion of the MMAs issued before an abandoned wait
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);  // [0] last arrival, [1..2] wait ok by tile parity, [3] phase ok
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int NP = CH.n_phases;
+  const uint64_t WL = CH.wait_ns;
   int* err = CH.ph[0].err;
   unsigned long long* tl = CH.tl ? CH.tl + static_cast<size_t>(c) * kTlWords : nullptr;
   if (tl && threadIdx.x == 0) {
@@ -510,6 +512,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 128);
     }
+    mbar_init(mdone, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         uint32_t a_only = 0;  // weights do not depend on earlier phases: stream them first
         for (; a_only < pre; ++a_only) {
           const uint32_t i = it + a_only, s = i % C::STAGES, r = i / C::STAGES;
-          if (i >= static_cast<uint32_t>(C::STAGES) && !mbar_wait(&empty[s], (r - 1) & 1)) {
+          if (i >= static_cast<uint32_t>(C::STAGES) && !mbar_wait(&empty[s], (r - 1) & 1, WL)) {
             ok = false;
             break;
           }
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             pdl_wait();
             pdl_launch_dependents();
           } else {
-            dep_ok = grid_wait(CH.bar + p - 1, G);
+            dep_ok = grid_wait(CH.bar + p - 1, G + CH.bar_extra, WL);
           }
         }
         tl_stamp(tl, 5 + 4 * p);
@@ -586,7 +589,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         }
         for (uint32_t k = pre; k < n; ++k) {
           const uint32_t s = it % C::STAGES, r = it / C::STAGES;
-          if (!mbar_wait(&empty[s], (r - 1) & 1)) {
+          if (!mbar_wait(&empty[s], (r - 1) & 1, WL)) {
             ok = false;
             break;
           }
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       // drain: every copy this thread issued has landed before the CTA may exit
       const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0;
       for (uint32_t i = first; i < it; ++i)
-        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1)) {
+        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, WL)) {
           raise_flag(err, kDevTimeout);
           break;
         }
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           const uint32_t ub = max(u0, static_cast<uint32_t>(t) * P.KB);
           const uint32_t ue = min(u1, static_cast<uint32_t>(t + 1) * P.KB);
           const int acc = lt & 1;
-          if (lt >= 2 && !mbar_wait(&tempty[acc], ((lt >> 1) - 1) & 1)) {
+          if (lt >= 2 && !mbar_wait(&tempty[acc], ((lt >> 1) - 1) & 1, WL)) {
             ok = false;
             break;
           }
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           const uint32_t idesc = P.b_lo ? C::IDESC2 : C::IDESC1;
           for (uint32_t u = ub; u < ue; ++u, ++i) {
             const uint32_t s = i % C::STAGES, r = i / C::STAGES;
-            if (!mbar_wait(&full[s], r & 1)) {
+            if (!mbar_wait(&full[s], r & 1, WL)) {
               ok = false;
               break;
             }
@@ -651,7 +654,13 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           if (ok) tc_commit(&tfull[acc]);
         }
       }
-      if (!ok) raise_flag(err, kDevTimeout);
+      if (!ok) {
+        raise_flag(err, kDevTimeout);
+        // MMAs already issued may still be writing the accumulators: wait for them before
+        // TMEM is released at the end of the kernel
+        tc_commit(mdone);
+        mbar_wait(mdone, 0, WL);
+      }
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -666,7 +675,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       int Gp;
       phase_units(P, c, G, U, u0, u1, Gp);
       if (p > 0) {
-        if (e == 0) s_misc[3] = grid_wait(CH.bar + p - 1, G) ? 1 : 0;
+        if (e == 0) s_misc[3] = grid_wait(CH.bar + p - 1, G + CH.bar_extra, WL) ? 1 : 0;
         named_bar_sync(1, 128);
         if (!s_misc[3]) {
           if (e == 0) raise_flag(err, kDevTimeout);
@@ -724,7 +733,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           const int acc = lt & 1;
           EpiPre pre;
           epilogue_prefetch<NB, C::MINB>(P, t, e, s_pos, pre);
-          if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1) ? 1 : 0;
+          if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1, WL) ? 1 : 0;
           named_bar_sync(1, 128);
           if (!s_misc[1 + acc]) {
             if (e == 0) raise_flag(err, kDevTimeout);
@@ -779,7 +788,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               to_rows<C::XLD>(v, m, e, xch, own);
             }
             if (e == 0) {
-              const bool ok = grid_wait(P.tile_cnt + t, cb - ca);
+              const bool ok = grid_wait(P.tile_cnt + t, cb - ca, WL);
               if (ok) P.tile_cnt[t] = 0;
               s_misc[0] = ok ? 1 : 0;
             }

@@ -8,6 +8,8 @@
 
 namespace dfl {
 
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
 // ---------------------------------------------------------------- weight-streaming GEMM
 // Y = X · Wᵀ over a weight matrix streamed once from HBM: the weight tile (128 output rows
 // x 64 k) is the 128-row A operand of tcgen05.mma, the <= 256 activation rows are the N
@@ -98,6 +100,8 @@ struct GemvChain {
   int* exit_cnt;  // [1]
   unsigned long long* tl;  // per-CTA timeline records (kTlWords each) or null
   int tl_id;               // launch id written into the records
+  unsigned long long wait_ns;  // limit of every wait in the kernel
+  int bar_extra;           // added to every grid-barrier target: 0, or 1 in the timeout self-test
 };
 
 // Timeline record of one CTA (kTlWords 64-bit words, %globaltimer nanoseconds):
@@ -130,6 +134,7 @@ struct AttnParams {
   float scale_log2;        // log2(e) / sqrt(d)
   unsigned long long* tl;  // timeline records (kTlWords per CTA) or null
   int tl_id;
+  unsigned long long wait_ns;  // limit of every wait in the kernel
 };
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
 int attn_set_attributes();

@@ -26,9 +26,9 @@ constexpr int kDevToken = 4;
 
 DEV void raise_flag(int* flag, int bits) { atomicOr(flag, bits); }
 
-// Every wait inside a kernel is bounded by this much wall time; past it the kernel sets
-// kDevTimeout and unwinds instead of spinning forever.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Every wait inside a kernel is bounded in wall time (a per-handle setting passed in the
+// launch parameters, kDefaultWaitLimitNs unless set); past it the kernel sets kDevTimeout
+// and unwinds instead of spinning forever.
 
 // ---------------------------------------------------------------- mbarrier
 DEV void mbar_init(uint64_t* bar, uint32_t count) {
@@ -55,13 +55,13 @@ DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of `bar` with the given parity to complete; false after kWaitLimitNs.
-DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase of `bar` with the given parity to complete; false after limit_ns.
+DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -94,16 +94,6 @@ DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, i
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global memory
-// into this CTA's shared memory, completing on `bar`.
-DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -186,9 +176,6 @@ DEV uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
   return r;
 }
-DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Split cluster barrier: arrive without ordering (after mbarrier initialisation, whose
 // fence publishes it), and wait (acquire) before the first access to a peer's memory.
 DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
@@ -205,54 +192,11 @@ DEV void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t byte
 DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the sources of this thread's committed bulk copies have been read.
 DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Store to a peer's shared memory (cluster address from mapa).
-DEV void st_shared_cluster_v2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-// Arrive on a peer's mbarrier, releasing this thread's earlier writes at cluster scope.
-DEV void mbar_arrive_remote(uint32_t mbar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster) : "memory");
-}
-// Wait for a phase of this CTA's mbarrier completed by arrivals from peers (acquire at
-// cluster scope); false after kWaitLimitNs.
-DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
 DEV uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-DEV float4 ld_shared_cluster_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-DEV float ld_shared_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // ---------------------------------------------------------------- timeline stamps
 DEV unsigned smid() {
   unsigned r;
@@ -262,8 +206,5 @@ DEV unsigned smid() {
 DEV void tl_stamp(unsigned long long* rec, int slot) {
   if (rec) rec[slot] = globaltimer_ns();
 }
-
-// ---------------------------------------------------------------- misc
-DEV float ld_cg_f32(const float* p) { return __ldcg(p); }
 
 }  // namespace dfl

@@ -58,7 +58,12 @@ extern "C" int dflash_verify_greedy_noalloc(const float* target_logits, const in
                                             int32_t block, int32_t vocab, int32_t* accept_len,
                                             int32_t* committed, int32_t* last_token, void* stream) {
   if (!target_logits || !accept_len || !committed || !last_token || (block > 1 && !drafted)) return DFLASH_E_INVAL;
-  if (batch < 1 || block < 1 || vocab < 2) return DFLASH_E_INVAL;
+  if (batch < 1 || block < 1 || vocab < 2 || vocab > DFLASH_NOALLOC_MAX_VOCAB) return DFLASH_E_INVAL;
+  // the logits are read 16 bytes at a time, the token arrays as 4-byte words
+  auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (misaligned(target_logits, 16) || misaligned(drafted, 4) || misaligned(accept_len, 4) ||
+      misaligned(committed, 4) || misaligned(last_token, 4))
+    return DFLASH_E_INVAL;
   if (batch > kMaxBatch || block > kMaxBlock) return DFLASH_E_CAPACITY;
   int* scratch = scratch_for_current_device();
   if (!scratch) return DFLASH_E_CUDA;

@@ -168,7 +168,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
 /* Greedy verification (bpdata.com DFlash article, introduction: the target accepts the
  * longest valid prefix): g_i = argmax target_logits[s][i] (lowest index on ties);
  * j = the number of leading i with drafted[s][i] == g_i (i < B-1); tau = j + 1.
- *   target_logits  fp32 [batch][B][V], finite
+ *   target_logits  fp32 [batch][B][V], finite, 16-byte aligned
  *   drafted        int32 [batch][B-1]
  *   accept_len     int32 [batch] out: tau in [1, B]
  *   committed      int32 [batch][B] out: g_0..g_{tau-1}, then -1
@@ -186,9 +186,38 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
 int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K, const void* X,
                        int32_t rows, float* Y, void* stream);
 
-/* Copy the device error flag to *flags (synchronises the handle's device); clear it when
- * `clear` is non-zero. */
-int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear);
+/* Copy the device error flag to *flags once the work queued on `stream` so far has
+ * finished (it waits for that stream only, not for the whole device). With `clear`
+ * non-zero it then zeroes the flag and every arrival counter in the workspace, which a
+ * kernel that gave up a bounded wait may have left part-counted; the handle is then
+ * usable again. Work of this handle must not be in flight on other streams meanwhile. */
+int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, void* stream);
+
+/* Per-handle settings (not part of the method; defaults suit GB300):
+ *   DFLASH_OPT_WAIT_LIMIT_NS  limit of every spin-wait inside a kernel (mbarriers, grid
+ *                             barriers, cluster peers), in ns, 1e5..6e10; default 2e9.
+ *                             Past it the kernel sets DFLASH_DEV_TIMEOUT and returns.
+ *   DFLASH_OPT_CHAIN_MAX      projections per persistent launch, 1..8; default 8
+ *   DFLASH_OPT_GEMV_VARIANT   weight-streaming variant of single-row-group passes, 0..5;
+ *                             default 3 (4 k-boxes per stage, 2 stages)
+ *   DFLASH_OPT_ATTN_SPLIT     CTAs per attention cluster, 0..16; 0 (default) chooses from
+ *                             the SM count
+ * Values out of range return DFLASH_E_INVAL and leave the setting unchanged. */
+#define DFLASH_OPT_WAIT_LIMIT_NS 1
+#define DFLASH_OPT_CHAIN_MAX 2
+#define DFLASH_OPT_GEMV_VARIANT 3
+#define DFLASH_OPT_ATTN_SPLIT 4
+int dflash_set_option(dflash_handle* h, int32_t option, int64_t value);
+int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value);
+
+/* Self-test of the bounded waits (not part of the method): launches one chained
+ * projection kernel (two plain projections through layer 0's output projection, writing
+ * only the draft's residual scratch) whose second phase waits for a grid-barrier count
+ * that no CTA reaches. Every waiting thread gives up after the handle's wait limit, the
+ * kernel sets DFLASH_DEV_TIMEOUT, waits (bounded) for its copies and MMAs in flight,
+ * releases its tensor memory and returns. Read and clear the flag with
+ * dflash_read_device_error(clear = 1) before the next call. Use a short wait limit. */
+int dflash_selftest_timeout(dflash_handle* h, void* stream);
 
 /* Number of kernel launches the last call on this handle made. */
 int32_t dflash_last_launch_count(const dflash_handle* h);
@@ -232,17 +261,23 @@ const char* dflash_status_string(int status);
  * and last_token[s] = g_{tau-1} is written to the caller's array. No handle is needed.
  * Its scratch (argmax partials and arrival counters, about 257 KB) is one fixed array
  * inside the library, which every GPU that loads the library keeps until the process
- * exits. Limits: batch <= DFLASH_NOALLOC_MAX_BATCH, block <= 16; larger sizes return
- * DFLASH_E_CAPACITY before anything is launched. It allocates no memory and calls no
+ * exits. Limits: batch <= DFLASH_NOALLOC_MAX_BATCH, block <= 16 (larger sizes return
+ * DFLASH_E_CAPACITY before anything is launched) and 2 <= vocab <= DFLASH_NOALLOC_MAX_VOCAB
+ * (DFLASH_E_INVAL otherwise). target_logits must be 16-byte aligned and the token
+ * arrays 4-byte aligned (DFLASH_E_INVAL otherwise). It allocates no memory and calls no
  * allocating routine.
  *   - The first call on each device looks up the array's device address (a host-side
- *     symbol lookup); make that first call before any stream capture.
+ *     symbol lookup). With lazy module loading (CUDA_MODULE_LOADING=LAZY) that lookup can
+ *     load the library's device code on that device, which allocates the array and the
+ *     code image. Make that first call before the region in which the caller may not
+ *     allocate, and before any stream capture.
  *   - All calls share the one array. Calls whose work overlaps on the GPU (different
  *     streams without ordering, or different host threads) race and give wrong results;
  *     order them on one stream. Each call clears the counters it needs, so the
  *     contents left by an earlier call do not matter. */
 #define DFLASH_NOALLOC_MAX_BATCH 64
 #define DFLASH_NOALLOC_MAX_CHUNKS 32
+#define DFLASH_NOALLOC_MAX_VOCAB (1 << 28)
 int dflash_verify_greedy_noalloc(const float* target_logits, const int32_t* drafted, int32_t batch,
                                  int32_t block, int32_t vocab, int32_t* accept_len, int32_t* committed,
                                  int32_t* last_token, void* stream);

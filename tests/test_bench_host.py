@@ -48,3 +48,21 @@ def test_traffic_withheld_when_sources_differ(tmp_path, monkeypatch):
         (tmp_path / src).write_bytes(open(os.path.join(bench.ROOT, src), "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.measured_traffic(t["launch"], t["workload"]) is None
+
+
+def test_reference_and_cuda_arms_print_the_same_config():
+    """Both arms describe the workload with one function, so their `config` objects match."""
+    w = WORKLOADS["qwen3-8b-b1-ctx2048-B16"]
+    c = bench.workload_config(w, 1, 0)
+    assert c["workload"] == w.name and c["block"] == 16 and c["ctx"] == 2048 and c["batch_per_gpu"] == 1
+    assert "l2" in c and c == bench.workload_config(w, 1, 0)
+
+
+def test_kv_counted_at_two_bytes_and_excess_reported_apart():
+    w = WORKLOADS["llama3.1-8b-L8-b4-ctx32768-B16"]
+    s = w.shape
+    kvb, _ = bench.attn_bytes_flops(s, w.batch, w.block, w.ctx)
+    n_kv = (w.ctx + w.block) * s.n_kv_heads * s.head_dim * w.batch
+    assert kvb - 8 * w.batch * w.block * s.n_heads * s.head_dim == 4 * n_kv
+    ex = bench.kv_storage_excess(s, w.batch, w.block, w.ctx, 4.0)
+    assert ex >= 2 * n_kv * s.n_layers

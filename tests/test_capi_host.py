@@ -94,3 +94,31 @@ def test_status_strings(L):
     assert L.dflash_status_string(0) == b"ok"
     assert L.dflash_status_string(-3) == b"capacity exceeded"
     assert L.dflash_status_string(123) == b"unknown status"
+
+
+def test_noalloc_verify_rejects_bad_arguments_before_any_launch(L):
+    """The allocation-free verifier checks alignment and sizes on the host: a misaligned
+    logits or token pointer, or a vocabulary beyond its stated maximum, returns
+    DFLASH_E_INVAL before the scratch array is looked up or anything is launched."""
+    ok16, ok4 = 1 << 20, 1 << 21   # never dereferenced: every call below fails its checks first
+    f = L.dflash_verify_greedy_noalloc
+    assert f(ok16 + 4, ok4, 1, 4, 1024, ok4, ok4, ok4, None) == -1      # logits not 16-byte aligned
+    assert f(ok16 + 8, ok4, 1, 4, 1023, ok4, ok4, ok4, None) == -1      # whatever the vocab
+    assert f(ok16, ok4 + 2, 1, 4, 1024, ok4, ok4, ok4, None) == -1      # drafted not 4-byte aligned
+    assert f(ok16, ok4, 1, 4, 1024, ok4 + 1, ok4, ok4, None) == -1      # accept_len
+    assert f(ok16, ok4, 1, 4, 1024, ok4, ok4 + 3, ok4, None) == -1      # committed
+    assert f(ok16, ok4, 1, 4, 1024, ok4, ok4, ok4 + 2, None) == -1      # last_token
+    assert f(ok16, ok4, 1, 4, (1 << 28) + 1, ok4, ok4, ok4, None) == -1  # vocab above the maximum
+    assert f(ok16, ok4, 1, 4, 1, ok4, ok4, ok4, None) == -1             # vocab below 2
+    assert f(ok16, ok4, 0, 4, 1024, ok4, ok4, ok4, None) == -1          # empty batch
+    assert f(ok16, ok4, 65, 4, 1024, ok4, ok4, ok4, None) == -3         # beyond the array
+    assert f(ok16, ok4, 1, 17, 1024, ok4, ok4, ok4, None) == -3
+
+
+def test_options_and_error_read_need_a_handle(L):
+    v = ctypes.c_int64(0)
+    assert L.dflash_set_option(None, B.OPT_CHAIN_MAX, 4) == -1
+    assert L.dflash_get_option(None, B.OPT_CHAIN_MAX, ctypes.byref(v)) == -1
+    assert L.dflash_selftest_timeout(None, None) == -1
+    f = ctypes.c_int32(0)
+    assert L.dflash_read_device_error(None, ctypes.byref(f), 0, None) == -1

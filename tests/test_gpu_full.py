@@ -35,30 +35,56 @@ def _draft(full, B):
     return drafted[0].cpu().numpy(), logits[0].cpu().numpy(), trace.cpu().numpy()
 
 
-def test_full_size_step_matches_oracle(full):
-    from gpu_util import check_draft, max_rel, LAYER_RTOL
+class _Prefilled:
+    pass
+
+
+@pytest.fixture(scope="module")
+def prefilled(full):
+    """The 2048-position context injected on both sides (checked element by element), and
+    the slot-0 token set: the state every block size below drafts from."""
+    from gpu_util import max_rel, LAYER_RTOL
     w, s, d = W_QWEN3_8B, full.s, full.drafter
-    B = w.block
-    hid = I.make_hidden(s, w.ctx + B, SEED, "full")
-    bits = I.bf16_bits(hid)
+    P = _Prefilled()
+    P.hid = I.make_hidden(s, w.ctx + w.block, SEED, "full")
+    P.bits = I.bf16_bits(P.hid)
     last = int(I.initial_tokens(1, s.vocab, SEED)[0])
     d.len.zero_()
     d.k_cache.zero_()
     d.v_cache.zero_()
-    full.gpu_inject(hid[:, : w.ctx].contiguous(), [w.ctx], rows_per_seq=w.ctx, batch=1)
+    full.gpu_inject(P.hid[:, : w.ctx].contiguous(), [w.ctx], rows_per_seq=w.ctx, batch=1)
     d.last_token[0] = last
-    st = full.oracle.new_sequence(full.cap, last)
-    full.oracle.inject(st, bits[:, : w.ctx])
+    P.st = full.oracle.new_sequence(full.cap, last)
+    full.oracle.inject(P.st, P.bits[:, : w.ctx])
     torch.cuda.synchronize()
     assert int(d.len[0]) == w.ctx and d.device_error() == 0
 
     def check_cache(n0, n1):
         k, v = full.gpu_cache(0, n1)
         for l in range(s.n_layers):
-            assert max_rel(k[l][n0:n1], st.k_cache[l][n0:n1]) <= LAYER_RTOL, f"K layer {l}"
-            assert max_rel(v[l][n0:n1], st.v_cache[l][n0:n1]) <= LAYER_RTOL, f"V layer {l}"
+            assert max_rel(k[l][n0:n1], P.st.k_cache[l][n0:n1]) <= LAYER_RTOL, f"K layer {l}"
+            assert max_rel(v[l][n0:n1], P.st.v_cache[l][n0:n1]) <= LAYER_RTOL, f"V layer {l}"
 
     check_cache(0, w.ctx)
+    P.check_cache = check_cache
+    return P
+
+
+@pytest.mark.parametrize("B", [4, 8, 12])
+def test_full_size_block_sweep_draft_matches_oracle(full, prefilled, B):
+    """The block-size sweep (B = 4, 8, 12 beside the 16 below) on the same injected context:
+    every layer's residual, the logits and the drafted tokens against the oracle."""
+    from gpu_util import check_draft
+    assert int(full.drafter.len[0]) == prefilled.st.length == W_QWEN3_8B.ctx
+    g_dr, g_lo, g_tr = _draft(full, B)
+    check_draft(full.oracle.draft(prefilled.st, B), g_dr, g_lo, g_tr)
+
+
+def test_full_size_step_matches_oracle(full, prefilled):
+    from gpu_util import check_draft
+    w, s, d = W_QWEN3_8B, full.s, full.drafter
+    B = w.block
+    st, hid, bits, check_cache = prefilled.st, prefilled.hid, prefilled.bits, prefilled.check_cache
 
     # first draft on the injected context
     g_dr, g_lo, g_tr = _draft(full, B)
@@ -165,9 +191,11 @@ def _run_sampled(w, seed, sampled, oracle_dtype=np.float64, chunk=4096):
 
 def test_batched_ragged_sampled_sequences_match_oracle():
     """Batch 32, context lengths uniform in [512, 8192], B = 16, per-sequence agreement
-    rates: the two shortest sequences against the oracle."""
+    rates. Sampled by index: one sequence in each group of eight (the rows of one 128-row
+    projection pass, and of one 256-row pass in pairs of groups), plus the sequence with
+    the longest context (the most key tiles per attention CTA)."""
     from synth import W_BATCHED
-    _run_sampled(W_BATCHED, 31, lambda ctx: np.argsort(ctx, kind="stable")[:2])
+    _run_sampled(W_BATCHED, 31, lambda ctx: sorted({3, 12, 21, 30, int(np.argmax(ctx))}))
 
 
 def test_long_context_llama_shaped_sequence_matches_oracle():

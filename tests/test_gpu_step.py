@@ -118,7 +118,7 @@ def test_inject_capacity_overflow_is_flagged(tiny):
 
 # ------------------------------------------------------------------ full step loop
 
-@pytest.mark.parametrize("B", [4, 1, 16])
+@pytest.mark.parametrize("B", [4, 1, 16, 8, 12])
 def test_step_loop_matches_oracle(tiny, B):
     """Prefill injection, then 3 steps of draft -> (synthetic target) -> verify -> inject,
     compared with the oracle at every stage. Verification is fed the oracle's drafts so a
@@ -194,3 +194,56 @@ def test_draft_rejects_misaligned_output_buffers(tiny):
     torch.cuda.synchronize()
     assert d.device_error() == 0
     assert bool(torch.isfinite(flat[: (B - 1) * s.vocab]).all())
+
+
+def test_verify_rejects_misaligned_logits(tiny):
+    """Target logits are read 16 bytes at a time: a pointer that is not 16-byte aligned is
+    refused before any launch (for every vocabulary size), and the handle stays usable."""
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    s, d = tiny.s, tiny.drafter
+    B = 4
+    flat = torch.zeros(B * s.vocab + 4, device="cuda")
+    drafted = torch.zeros(1, B - 1, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    com = torch.zeros(1, B, dtype=torch.int32, device="cuda")
+    for off in (1, 2, 3):
+        with pytest.raises(BND.DFlashError) as ei:
+            d.verify(flat[off: off + B * s.vocab].view(1, B, s.vocab), drafted, 1, B, acc, com)
+        assert ei.value.status == BND.DFLASH_E_INVAL
+    d.verify(flat[4: 4 + B * s.vocab].view(1, B, s.vocab), drafted, 1, B, acc, com)
+    torch.cuda.synchronize()
+    assert 1 <= int(acc[0]) <= B
+
+
+def test_options_round_trip(tiny):
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    d = tiny.drafter
+    assert d.get_option(BND.OPT_WAIT_LIMIT_NS) == 2_000_000_000
+    assert d.get_option(BND.OPT_CHAIN_MAX) == 8
+    for opt, bad in ((BND.OPT_WAIT_LIMIT_NS, 10), (BND.OPT_CHAIN_MAX, 9), (BND.OPT_GEMV_VARIANT, 6),
+                     (BND.OPT_ATTN_SPLIT, 17), (99, 1)):
+        with pytest.raises(BND.DFlashError):
+            d.set_option(opt, bad)
+    d.set_option(BND.OPT_CHAIN_MAX, 3)
+    assert d.get_option(BND.OPT_CHAIN_MAX) == 3
+    d.set_option(BND.OPT_CHAIN_MAX, 8)
+
+
+def test_bounded_wait_unwinds_and_the_handle_recovers(tiny):
+    """A chained projection kernel whose grid barrier can never be met (the self-test
+    entry) gives up after the handle's 1 ms wait limit: the call returns, the timeout bit
+    is set, and once it is read and cleared the same handle runs a full step loop that
+    matches the oracle (tensor memory was released and the counters were reset)."""
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    d = tiny.drafter
+    d.device_error()
+    d.set_option(BND.OPT_WAIT_LIMIT_NS, 1_000_000)
+    try:
+        d.selftest_timeout()
+        torch.cuda.synchronize()
+        flags = d.device_error(clear=True)
+        assert flags & BND.DEV_TIMEOUT
+    finally:
+        d.set_option(BND.OPT_WAIT_LIMIT_NS, 2_000_000_000)
+    assert d.device_error() == 0
+    _step_loop(tiny, 4)

@@ -58,6 +58,52 @@ def test_noalloc_matches_regular_entry_on_consecutive_calls(drafter, batch, bloc
         assert int(acc_a.min()) >= 1
 
 
+@pytest.fixture(scope="module")
+def wide_vocab():
+    """A drafter handle whose vocabulary is the Qwen3-8B-sized one (151 936 logits per row),
+    so the regular entry point and the allocation-free one both split a row into many
+    chunks; max_batch 64 covers the fixed array's largest batch."""
+    from dataclasses import replace
+    from block_diffusion_drafter_kv_gb300 import binding as B
+    from block_diffusion_drafter_kv_gb300.build import build
+    from synth import TINY
+    from synth import inputs as I
+    build()
+    s = replace(TINY, vocab=151936)
+    return B.Drafter(s, I.make_weights(s, 5).to("cuda"), max_block=16, max_batch=64, kv_capacity=64)
+
+
+@pytest.mark.parametrize("batch,block", [(32, 16), (64, 16), (3, 5)])
+def test_noalloc_multi_chunk_rows_match_oracle_and_regular_entry(wide_vocab, batch, block):
+    """At V = 151 936 each row is reduced in several chunks (up to 32) through the fixed
+    array's layout; batch 64 with B = 16 fills the array to its stated limit. Two calls in
+    a row must both equal the oracle's greedy verification and the regular entry point."""
+    from block_diffusion_drafter_kv_gb300 import binding as B
+    from oracle.dflash_ref import verify_greedy
+    vocab = wide_vocab.shape.vocab
+    rng = np.random.default_rng(batch * 7 + block)
+    for call in range(2):
+        T, d = _inputs(rng, batch, block, vocab)
+        T[batch - 1, block - 1, vocab - 1] = T[batch - 1, block - 1].max() + 2.0   # the last logit wins a row
+        acc = torch.full((batch,), -9, dtype=torch.int32, device="cuda")
+        com = torch.full((batch, block), -9, dtype=torch.int32, device="cuda")
+        last = torch.full((batch,), -9, dtype=torch.int32, device="cuda")
+        B.verify_greedy_noalloc(T, d, batch, block, acc, com, last)
+        acc_b = torch.full((batch,), -9, dtype=torch.int32, device="cuda")
+        com_b = torch.full((batch, block), -9, dtype=torch.int32, device="cuda")
+        wide_vocab.verify(T, d, batch, block, acc_b, com_b)
+        torch.cuda.synchronize()
+        assert torch.equal(acc, acc_b) and torch.equal(com, com_b)
+        assert torch.equal(last, wide_vocab.last_token[:batch])
+        Tn, dn = T.cpu().numpy(), d.cpu().numpy()
+        a, c, l = acc.cpu().numpy(), com.cpu().numpy(), last.cpu().numpy()
+        for q in range(batch):
+            r = verify_greedy(Tn[q], dn[q])
+            assert a[q] == r.accept_len, (call, q)
+            assert list(c[q, : r.accept_len]) == list(r.committed) and (c[q, r.accept_len:] == -1).all()
+            assert l[q] == r.last_token
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
     from block_diffusion_drafter_kv_gb300 import binding as B
     L = B.lib()
