@@ -65,10 +65,9 @@ def peaks():
 def proj_bytes_flops(s, batch, B, tau):
     """Algorithmic (bytes, flops) of each projection: the weight read once, the activation
     rows read once, the outputs written once. bf16 activation operands are two planes
-    (high and low, 4 bytes per value); q is fp32; K and V cache entries count 2 bytes each
-    (bf16, the method's KV; the library's fp32 K storage is excess traffic, reported
-    apart); the residual stream is fp32 (read and written by O and down). FLOPs count one
-    product per weight and row (the low plane's second product is not counted)."""
+    (high and low, 4 bytes per value); q and the K and V cache entries are fp16 (2 bytes);
+    the residual stream is fp32 (read and written by O and down). FLOPs count one product
+    per weight and row (the low plane's second product is not counted)."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     rows = batch * B
     kin = s.n_taps * s.target_hidden
@@ -79,7 +78,7 @@ def proj_bytes_flops(s, batch, B, tau):
     return {
         "fc": (2 * H * kin + 2 * tau * kin + 4 * tau * H, 2 * tau * H * kin),
         "kv": (2 * kv * H + 4 * tau * H + 2 * tau * kv, 2 * tau * kv * H),
-        "qkv": (2 * nqkv * H + 4 * rows * H + rows * (4 * nqd + 4 * kvd), 2 * rows * nqkv * H),
+        "qkv": (2 * nqkv * H + 4 * rows * H + rows * (2 * nqd + 4 * kvd), 2 * rows * nqkv * H),
         "o": (2 * H * nqd + 4 * rows * nqd + 12 * rows * H, 2 * rows * H * nqd),
         "gateup": (2 * 2 * I * H + 4 * rows * (H + I), 2 * rows * 2 * I * H),
         "down": (2 * H * I + 4 * rows * I + 12 * rows * H, 2 * rows * H * I),
@@ -88,10 +87,10 @@ def proj_bytes_flops(s, batch, B, tau):
 
 
 def attn_bytes_flops(s, batch, B, n_ctx):
-    """K and V read once per layer per sequence (context plus block keys) at 2 bytes per
-    element each (bf16, the method's KV), q (fp32) read, o (two bf16 planes) written."""
+    """K and V (fp16) read once per layer per sequence (context plus block keys), q (fp16)
+    read, o (two bf16 planes) written."""
     kvb = 4 * (n_ctx + B) * s.n_kv_heads * s.head_dim * batch
-    qo = 8 * batch * B * s.n_heads * s.head_dim
+    qo = 6 * batch * B * s.n_heads * s.head_dim
     fl = 4 * batch * B * s.n_heads * s.head_dim * (n_ctx + B)
     return kvb + qo, fl
 
@@ -151,16 +150,6 @@ def measured_traffic(launch, workload):
         with open(os.path.join(ROOT, src), "rb") as f:
             h.update(f.read())
     return t["traffic_bytes"] if h.hexdigest() == t["sources_sha256"] else None
-
-
-def kv_storage_excess(s, batch, B, n_ctx, tau):
-    """Bytes per step the library moves beyond the method's bf16 K/V because it stores K
-    as fp32 (TF32-rounded): 2 more bytes per K element read by attention in every layer,
-    and per K element written by injection and by the block's Q/K/V projection."""
-    kvd = s.n_kv_heads * s.head_dim
-    read = 2 * (n_ctx + B) * kvd * batch * s.n_layers
-    written = 2 * (tau + B) * kvd * batch * s.n_layers
-    return read + written
 
 
 def step_bytes_flops(s, batch, B, n_ctx, tau):
@@ -747,7 +736,6 @@ def run_cuda(a):
             "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
             "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block,
             "draft_flatness": (max(draft_by_block.values()) / min(draft_by_block.values())) if draft_by_block else None,
-            "kv_storage_excess_bytes_per_step": kv_storage_excess(s, batch, B, n_avg, tau_avg),
             "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,
             "clocks": clk, "device_error": err,

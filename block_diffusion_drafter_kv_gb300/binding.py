@@ -139,9 +139,9 @@ class Drafter:
         dev = weights.w_fc.device
         s = shape
         self.k_cache = torch.zeros(s.n_layers, max_batch, kv_capacity, s.n_kv_heads, s.head_dim,
-                                   dtype=torch.float32, device=dev)   # TF32-rounded values
+                                   dtype=torch.float16, device=dev)
         self.v_cache = torch.zeros(s.n_layers, max_batch, kv_capacity, s.n_kv_heads, s.head_dim,
-                                   dtype=torch.bfloat16, device=dev)
+                                   dtype=torch.float16, device=dev)
         self.len = torch.zeros(max_batch, dtype=torch.int32, device=dev)
         self.last_token = torch.zeros(max_batch, dtype=torch.int32, device=dev)
         nbytes = self.L.dflash_workspace_size(ctypes.byref(self.cfg))

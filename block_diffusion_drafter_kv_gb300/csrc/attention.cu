@@ -10,9 +10,8 @@
 // Split-KV flash decoding: one thread-block cluster per (sequence, KV head); the CTAs of
 // the cluster split the key range. In a CTA, warp w serves query head g*group + w for all
 // (<= 16) block slots, so the group's query heads share every K/V tile staged in shared
-// memory by TMA. QKᵀ runs on the tensor cores in TF32 against the fp32 K cache and PV in
-// bf16 against the bf16 V cache, both accumulating in fp32, with an online softmax in
-// registers. The CTAs' partial (max, sum, output) are merged through distributed shared
+// memory by TMA. QKᵀ and PV run on the tensor cores with fp16 operands (q, the fp16 K and V
+// caches, the probabilities) accumulating in fp32, with an online softmax in registers. The CTAs' partial (max, sum, output) are merged through distributed shared
 // memory in a fixed order, so no partials touch HBM. The output is written as a high bf16
 // plane and a low plane (the bf16 of the remainder) for the output projection.
 #include "attn_tile.cuh"
@@ -26,10 +25,10 @@ namespace {
 constexpr int KT = kAttnKeys;  // keys per tile
 constexpr int STAGES = 3;
 
-// Offset of the merge inputs from the 1024-aligned base: the ring of fp32 K + bf16 V tiles,
-// its full/empty barriers, the merge barrier and two flags.
+// Offset of the merge inputs from the 1024-aligned base: the ring of fp16 K + V tiles, its
+// full/empty barriers, the merge barrier and two flags.
 __host__ __device__ constexpr int attn_recv_offset(int D) {
-  return (STAGES * KT * D * 6 + (2 * STAGES + 1) * 8 + 8 + 15) / 16 * 16;
+  return (STAGES * KT * D * 4 + (2 * STAGES + 1) * 8 + 8 + 15) / 16 * 16;
 }
 
 }  // namespace
@@ -42,8 +41,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     tl[1] = smid();
     tl_stamp(tl, 2);
   }
-  constexpr int K_BYTES = KT * D * 4;  // fp32 K tile
-  constexpr int V_BYTES = KT * D * 2;  // bf16 V tile
+  constexpr int K_BYTES = KT * D * 2;  // fp16 K tile
+  constexpr int V_BYTES = KT * D * 2;  // fp16 V tile
   constexpr int TILE_BYTES = K_BYTES + V_BYTES;
   constexpr int NT_D = D / 8;   // n-tiles over d in the output
   extern __shared__ uint8_t smem_raw[];
@@ -106,7 +105,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     const int row = key_row0 + (t0 + i) * KT;
     mbar_arrive_expect_tx(&full[st], TILE_BYTES);
 #pragma unroll
-    for (int b = 0; b < D / 32; ++b) tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 32, g, row, pol);
+    for (int b = 0; b < D / 64; ++b) tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
 #pragma unroll
     for (int b = 0; b < D / 64; ++b) tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
   };

@@ -1,14 +1,14 @@
-// Flash-attention building blocks shared by the standalone block-attention kernel and
-// the attention phase of the chained projection kernel (sm_103a).
+// Flash-attention building blocks of the block-attention kernel (sm_103a).
 //
 // One warp owns 16 query rows (the block's slots for one query head) and walks key tiles
-// of 64 staged in shared memory by TMA: K as fp32 (128-byte swizzled boxes of 64 keys x 32
-// dims), V as bf16 (boxes of 64 keys x 64 dims). S = Q Kᵀ runs on the tensor cores in TF32
-// (mma.sync m16n8k8; q and K are stored already rounded to TF32), because the scores are
-// the step's most rounding-sensitive quantity: the attention output is a weighted mean of
-// values with much cancellation, so small score errors grow in relative terms. O += P V
-// runs in bf16 (mma.sync m16n8k16), all accumulation in fp32, with an online softmax in
-// registers in log2 units.
+// of 64 staged in shared memory by TMA: K and V as fp16, each in boxes of 64 keys x 64 dims
+// (128-byte rows, 128-byte swizzle). S = Q Kᵀ and O += P V run on the tensor cores as
+// mma.sync m16n8k16 with fp16 operands and fp32 accumulation, with an online softmax in
+// registers in log2 units. fp16 carries 11 significant bits, the same as TF32: the scores
+// are the step's most rounding-sensitive quantity (the attention output is a weighted mean
+// of values with much cancellation, so small score errors grow in relative terms), and
+// fp16 q, K, P and V keep them, and the products with V, at that precision while K and V
+// cost 2 bytes per element.
 #pragma once
 
 #include "ptx.cuh"
@@ -27,58 +27,48 @@ DEV void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+DEV void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-DEV void mma_tf32_1688(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-DEV uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+DEV uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte address of element (key, d) in a bf16 V tile: D/64 TMA boxes of 64 keys x 128 bytes,
-// each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
+// Byte address of element (key, d) in an fp16 K or V tile: D/64 TMA boxes of 64 keys x 128
+// bytes, each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk
+// c ^ (r & 7)).
 DEV uint32_t kv_addr(uint32_t base, int key, int d) {
   const int box = d >> 6, dd = d & 63;
   return base + box * (kAttnKeys * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
 }
-// The same for an fp32 K tile: D/32 boxes of 64 keys x 128 bytes (32 dims); d a multiple of 4.
-DEV uint32_t k32_addr(uint32_t base, int key, int d) {
-  const int box = d >> 5, dd = d & 31;
-  return base + box * (kAttnKeys * 128) + key * 128 + ((((dd >> 2) ^ (key & 7))) << 4);
-}
 
 template <int D>
 struct FaState {
-  uint32_t qa[D / 8][4];   // Q fragments (TF32 A operand, one per 8 dims)
+  uint32_t qa[D / 16][4];  // Q fragments (fp16 A operand, one per 16 dims)
   float m[2], l[2];        // running max (log2 units) and sum for rows r0 and r0 + 8
   float o[D / 8][4];       // unnormalised output accumulators
 };
 
 // Q rows for one query head: row i (< B) is query[row0 + i][head*D .. +D); rows >= B are zero.
 template <int D>
-DEV void fa_begin(FaState<D>& st, const float* q, size_t row0, size_t ld, int head, int B, int lane) {
-  const int r0 = lane >> 2, kc = lane & 3;
-  const float* q0 = q + (row0 + r0) * ld + static_cast<size_t>(head) * D;
-  const float* q1 = q0 + 8 * ld;
+DEV void fa_begin(FaState<D>& st, const __half* q, size_t row0, size_t ld, int head, int B, int lane) {
+  const int r0 = lane >> 2, kc = (lane & 3) * 2;
+  const __half* q0 = q + (row0 + r0) * ld + static_cast<size_t>(head) * D;
+  const __half* q1 = q0 + 8 * ld;
   const bool v0 = r0 < B, v1 = r0 + 8 < B;
+  auto ld2 = [](const __half* p) { return __ldcg(reinterpret_cast<const unsigned int*>(p)); };
 #pragma unroll
-  for (int kk = 0; kk < D / 8; ++kk) {
-    const int c = kk * 8 + kc;
-    st.qa[kk][0] = v0 ? __float_as_uint(__ldcg(q0 + c)) : 0u;
-    st.qa[kk][1] = v1 ? __float_as_uint(__ldcg(q1 + c)) : 0u;
-    st.qa[kk][2] = v0 ? __float_as_uint(__ldcg(q0 + c + 4)) : 0u;
-    st.qa[kk][3] = v1 ? __float_as_uint(__ldcg(q1 + c + 4)) : 0u;
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int c = kk * 16 + kc;
+    st.qa[kk][0] = v0 ? ld2(q0 + c) : 0u;
+    st.qa[kk][1] = v1 ? ld2(q1 + c) : 0u;
+    st.qa[kk][2] = v0 ? ld2(q0 + c + 8) : 0u;
+    st.qa[kk][3] = v1 ? ld2(q1 + c + 8) : 0u;
   }
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.f;
@@ -87,7 +77,7 @@ DEV void fa_begin(FaState<D>& st, const float* q, size_t row0, size_t ld, int he
 }
 
 // One tile of 64 keys starting at key0 (keys >= nkeys are masked out); kb / vb are the
-// shared-memory addresses of the staged fp32 K and bf16 V tiles.
+// shared-memory addresses of the staged fp16 K and V tiles.
 template <int D>
 DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, float scale_log2, int lane) {
   constexpr int NT_D = D / 8;
@@ -95,19 +85,20 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
   float sc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-  // ldmatrix on 16-bit pairs hands lane t the 32-bit element (row t/4, column t%4) of each
-  // 8 x (4 x 32-bit) matrix: with rows = keys and columns = 4 dims, that is the TF32 B
-  // fragment (k = t%4, n = t/4). Matrices 0..3: dims d0, d0+4 (step kk), d0+8, d0+12 (kk+1).
+  // S = Q Kᵀ. ldmatrix hands lane t row t/4, halves 2(t%4)..+1 of each 8 x 8 matrix: with
+  // rows = keys and columns = 8 dims that is the B fragment (k = dims, n = keys). Matrices
+  // 0..3: keys 0-7 dims lo, keys 0-7 dims hi, keys 8-15 dims lo, keys 8-15 dims hi.
 #pragma unroll
-  for (int kk = 0; kk < D / 8; kk += 2) {
+  for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      const int key = np * 8 + (lane & 7);
-      const int d = kk * 8 + (lane >> 3) * 4;
+    for (int np = 0; np < 4; ++np) {
+      const int mi = lane >> 3;
+      const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
+      const int d = kk * 16 + (mi & 1) * 8;
       uint32_t b[4];
-      ldsm_x4(k32_addr(kb, key, d), b);
-      mma_tf32_1688(sc[np], st.qa[kk], b[0], b[1]);
-      mma_tf32_1688(sc[np], st.qa[kk + 1], b[2], b[3]);
+      ldsm_x4(kv_addr(kb, key, d), b);
+      mma_f16_16816(sc[2 * np], st.qa[kk], b[0], b[1]);
+      mma_f16_16816(sc[2 * np + 1], st.qa[kk], b[2], b[3]);
     }
   }
   // scale to log2 units, mask keys past the end, online softmax
@@ -156,10 +147,10 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
     uint32_t pa[4];
-    pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-    pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-    pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-    pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+    pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
+    pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
+    pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+    pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
     for (int dp = 0; dp < D / 16; ++dp) {
       const int mi = lane >> 3;
@@ -167,8 +158,8 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
       const int d = dp * 16 + (mi >> 1) * 8;
       uint32_t b[4];
       ldsm_x4_trans(kv_addr(vb, key, d), b);
-      mma_bf16_16816(st.o[2 * dp], pa, b[0], b[1]);
-      mma_bf16_16816(st.o[2 * dp + 1], pa, b[2], b[3]);
+      mma_f16_16816(st.o[2 * dp], pa, b[0], b[1]);
+      mma_f16_16816(st.o[2 * dp + 1], pa, b[2], b[3]);
     }
   }
 }

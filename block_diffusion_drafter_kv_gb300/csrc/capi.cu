@@ -72,7 +72,7 @@ WsLayout layout_of(const dflash_config& c) {
   L.cfeat = take(static_cast<size_t>(2 * kMaxPassRows) * H * 2);
   L.x = take(R * H * 4);
   L.xg = take(2 * R * H * 2);
-  L.q = take(R * nq * d * 4);
+  L.q = take(R * nq * d * 2);
   L.o = take(2 * R * nq * d * 2);
   L.act = take(2 * R * I * 2);
   L.vpart_v = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
@@ -119,24 +119,14 @@ bool enc3d_hidden(CUtensorMap* m, const void* base, uint64_t Ht, uint64_t rows, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One layer's fp32 K cache [rows = max_batch*cap][nkv][d], box 32 (d, 128 bytes) x 1 head x 64 keys.
-bool enc3d_cache_f32(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
-  cuuint64_t dims[3] = {d, nkv, rows};
-  cuuint64_t strides[2] = {d * 4, nkv * d * 4};
-  cuuint32_t box[3] = {32, 1, 64};
-  cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// One layer's bf16 V cache [rows = max_batch*cap][nkv][d], box 64 (d) x 1 head x 64 keys.
+// One layer's fp16 K or V cache [rows = max_batch*cap][nkv][d], box 64 (d, 128 bytes) x 1 head
+// x 64 keys.
 bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
   cuuint64_t dims[3] = {d, nkv, rows};
   cuuint64_t strides[2] = {d * 2, nkv * d * 2};
   cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -174,8 +164,8 @@ struct dflash_handle {
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
   // bound state
   bool bound = false;
-  float* kc = nullptr;
-  __nv_bfloat16* vc = nullptr;
+  __half* kc = nullptr;
+  __half* vc = nullptr;
   int* len = nullptr;
   int* last_token = nullptr;
   uint8_t* ws = nullptr;
@@ -356,8 +346,8 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
   const auto& c = h->cfg;
   const WsLayout L = layout_of(c);
   if (workspace_bytes < L.total) return DFLASH_E_CAPACITY;
-  h->kc = static_cast<float*>(k_cache);
-  h->vc = static_cast<__nv_bfloat16*>(v_cache);
+  h->kc = static_cast<__half*>(k_cache);
+  h->vc = static_cast<__half*>(v_cache);
   h->len = len;
   h->last_token = last_token;
   h->ws = static_cast<uint8_t*>(workspace);
@@ -391,7 +381,7 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
   const size_t layer_elems = static_cast<size_t>(c.max_batch) * c.kv_capacity * c.n_kv_heads * d;
   for (int l = 0; l < c.n_layers && ok; ++l) {
     const uint64_t rows = static_cast<uint64_t>(c.max_batch) * c.kv_capacity;
-    ok = enc3d_cache_f32(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
+    ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
          enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, rows);
   }
   if (!ok) return DFLASH_E_CUDA;
@@ -555,7 +545,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
       P.ss_parts = H / 128;
     }
     P.ss_stride = R;
-    P.qf = h->at<float>(h->L.q);
+    P.qh = h->at<__half>(h->L.q);
     P.yb_ld = c.n_heads * d;
     P.rope_cos = h->at<float>(h->L.rope_cos);
     P.rope_sin = h->at<float>(h->L.rope_sin);
@@ -649,7 +639,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     AttnParams A{};
     A.kmap = h->m_kcache[l];
     A.vmap = h->m_vcache[l];
-    A.q = h->at<float>(h->L.q);
+    A.q = h->at<__half>(h->L.q);
     A.o = h->at<__nv_bfloat16>(h->L.o);
     A.o_lo = R;
     A.len = h->len;

@@ -66,13 +66,14 @@ struct GemvCfg {
 DEV float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 DEV __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
 
-
-// fp32 rounded to TF32 (10-bit mantissa, nearest, ties away), the operand precision of the
-// attention score MMA; values stored this way are used by it exactly.
-DEV float to_tf32(float v) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-  return __uint_as_float(r);
+// 16 values as fp16 (round to nearest even), 32 bytes at p.
+DEV void st16_half(__half* p, const float (&v)[16]) {
+  uint4 b[2];
+  __half2* h = reinterpret_cast<__half2*>(b);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) h[k] = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+  reinterpret_cast<uint4*>(p)[0] = b[0];
+  reinterpret_cast<uint4*>(p)[1] = b[1];
 }
 
 // CTA whose unit range contains unit u (units split as floor(c*U/G)).
@@ -321,27 +322,12 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
         }
       }
       if (is_q) {
-        if (gr < P.n_valid) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) val[k] = to_tf32(val[k]);
-          st16(P.qf + static_cast<size_t>(gr) * P.yb_ld + feat0, val);
-        }
+        if (gr < P.n_valid) st16_half(P.qh + static_cast<size_t>(gr) * P.yb_ld + feat0, val);
       } else if (s_pos[lr] >= 0) {
         const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
         const size_t off =
             ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr]) * P.cap + s_pos[lr]) * row_elems + feat0;
-        if (is_v) {
-          uint4 b[2];
-          __nv_bfloat16* bv = reinterpret_cast<__nv_bfloat16*>(b);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) bv[k] = f2bf(val[k]);
-          reinterpret_cast<uint4*>(P.vc + off)[0] = b[0];
-          reinterpret_cast<uint4*>(P.vc + off)[1] = b[1];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) val[k] = to_tf32(val[k]);
-          st16(P.kc + off, val);
-        }
+        st16_half((is_v ? P.vc : P.kc) + off, val);
       }
     } break;
 
@@ -487,7 +473,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* mdone = tempty + 2;  // completion of the MMAs issued before an abandoned wait
+  uint64_t* mdone = tempty + 2;  // completion of every MMA this CTA issued
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);  // [0] last arrival, [1..2] wait ok by tile parity, [3] phase ok
 
@@ -654,13 +640,12 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           if (ok) tc_commit(&tfull[acc]);
         }
       }
-      if (!ok) {
-        raise_flag(err, kDevTimeout);
-        // MMAs already issued may still be writing the accumulators: wait for them before
-        // TMEM is released at the end of the kernel
-        tc_commit(mdone);
-        mbar_wait(mdone, 0, WL);
-      }
+      if (!ok) raise_flag(err, kDevTimeout);
+      // Every MMA issued has completed before TMEM is released at the end of the kernel.
+      // (Normally the epilogue has already waited for them; after an abandoned wait it may
+      // not have.)
+      tc_commit(mdone);
+      if (!mbar_wait(mdone, 0, WL)) raise_flag(err, kDevTimeout);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -67,14 +68,14 @@ struct GemvParams {
   __nv_bfloat16* yb;        // FC: cfeat; RESID: xg; SWIGLU: act (bf16 high plane)
   int yb_ld;
   int yb_lo;                // rows from a yb row to its low plane; 0: write the high plane only
-  float* qf;                // QKV: post-RoPE queries, fp32 rounded to TF32, [rows][nq*d]
+  __half* qh;               // QKV: post-RoPE queries, fp16, [rows][nq*d]
   float* trace;             // RESID: optional residual trace
   // RoPE and caches
   const float* rope_cos;    // [cap][d/2]
   const float* rope_sin;
   int d;
-  float* kc;                // K cache, fp32 rounded to TF32: [L][max_batch][cap][nkv][d]
-  __nv_bfloat16* vc;        // V cache, bf16, same layout
+  __half* kc;               // K cache (post-RoPE), fp16: [L][max_batch][cap][nkv][d]
+  __half* vc;               // V cache, fp16, same layout
   int nkv, cap, max_batch, layer;
   int* len;
   const int* n_new;
@@ -123,9 +124,9 @@ int gemv_set_attributes();
 
 // ---------------------------------------------------------------- block attention
 struct AttnParams {
-  CUtensorMap kmap;  // 3-D over this layer's fp32 K cache: {d, nkv, max_batch*cap}, box {32, 1, 64}
-  CUtensorMap vmap;  // 3-D over this layer's bf16 V cache: box {64, 1, 64}
-  const float* q;    // [rows][nq*d], row = s*B + i, post-RoPE, TF32-rounded
+  CUtensorMap kmap;  // 3-D over this layer's fp16 K cache: {d, nkv, max_batch*cap}, box {64, 1, 64}
+  CUtensorMap vmap;  // 3-D over this layer's fp16 V cache: box {64, 1, 64}
+  const __half* q;   // [rows][nq*d], row = s*B + i, post-RoPE, fp16
   __nv_bfloat16* o;  // [rows][nq*d] high plane; the low plane follows o_lo rows further on
   int o_lo;
   const int* len;

