@@ -18,7 +18,7 @@ DFLASH_E_INVAL = -1
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: "capacity exceeded",
           -4: "CUDA error", -5: "state not bound"}
 DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4
-OPT_WAIT_LIMIT_NS, OPT_CHAIN_MAX, OPT_GEMV_VARIANT, OPT_ATTN_SPLIT = 1, 2, 3, 4
+OPT_WAIT_LIMIT_NS, OPT_CHAIN_MAX, OPT_GEMV_VARIANT, OPT_ATTN_SPLIT, OPT_ATTN_KEY_GROUPS = 1, 2, 3, 4, 5
 
 
 class DflashConfig(ctypes.Structure):

@@ -8,9 +8,11 @@
 // the key range is one contiguous run.
 //
 // Split-KV flash decoding: one thread-block cluster per (sequence, KV head); the CTAs of
-// the cluster split the key range. In a CTA, warp w serves query head g*group + w for all
-// (<= 16) block slots, so the group's query heads share every K/V tile staged in shared
-// memory by TMA. QKᵀ and PV run on the tensor cores with fp16 operands (q, the fp16 K and V
+// the cluster split the key range. In a CTA, warp w serves query head g*group + w % group for
+// all (<= 16) block slots, so the group's query heads share every K/V tile staged in shared
+// memory by TMA. With two key groups (2 * group warps), warps w and w + group serve the same
+// head and take alternate tiles, so each SM sub-partition has two independent MMA chains to
+// interleave; their states are combined in shared memory after the key loop. QKᵀ and PV run on the tensor cores with fp16 operands (q, the fp16 K and V
 // caches, the probabilities) accumulating in fp32, with an online softmax in registers. The CTAs' partial (max, sum, output) are merged through distributed shared
 // memory in a fixed order, so no partials touch HBM. The output is written as a high bf16
 // plane and a low plane (the bf16 of the remainder) for the output projection.
@@ -54,8 +56,9 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   float* s_stage = reinterpret_cast<float*>(smem);  // after the key loop: partials by merging CTA
   float* s_recv = reinterpret_cast<float*>(smem + attn_recv_offset(D));
 
-  const int nw = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = P.nq / P.nkv;                   // warps per key group: the GQA group
+  const int KW = (blockDim.x >> 5) / nw;         // key groups (1 or 2)
+  const int warp = (threadIdx.x >> 5) % nw, kg = (threadIdx.x >> 5) / nw, lane = threadIdx.x & 31;
   const int g = blockIdx.y, seq = blockIdx.z;
   const int S = gridDim.x;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -122,6 +125,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     for (int i = 0; i < pre; ++i)
       if ((t0 + i + 1) * KT > len) issue(i, pol);
   }
+  int issued = pre;  // thread 0: tiles issued so far (in order)
 
   // Q fragments of this warp's head: rows = block slots (>= B are zero).
   const int nq = P.nq;
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   FaState<D> fa;
   fa_begin<D>(fa, P.q, static_cast<size_t>(seq) * B, static_cast<size_t>(nq) * D, h, B, lane);
 
-  for (int i = 0; i < n; ++i) {
+  for (int i = kg; i < n; i += KW) {
     const int st = i % STAGES;
     if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1, P.wait_ns)) {
       s_flag[0] = 1;
@@ -141,19 +145,63 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     fa_tile<D>(fa, kb, kb + K_BYTES, (t0 + i) * KT, nkeys, P.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
-    if (threadIdx.x == 0 && i + STAGES < n) {
-      if (!s_flag[0] && !mbar_wait(&empty[st], (i / STAGES) & 1, P.wait_ns)) {
-        s_flag[0] = 1;
-        raise_flag(P.err, kDevTimeout);
+    // Thread 0 refills the ring in tile order: every tile up to the other key group's next
+    // one plus the ring depth. Tile j reuses the stage of tile j - STAGES, consumed either
+    // by this warp (tile i) or by the other key group (tile i + 1, already issued), so
+    // the wait always ends.
+    if (threadIdx.x == 0) {
+      while (issued < n && issued <= i + KW + STAGES - 1 && !s_flag[0]) {
+        const int sj = issued % STAGES;
+        if (!mbar_wait(&empty[sj], ((issued / STAGES) - 1) & 1, P.wait_ns)) {
+          s_flag[0] = 1;
+          raise_flag(P.err, kDevTimeout);
+          break;
+        }
+        issue(issued, policy_evict_last());
+        ++issued;
       }
-      if (!s_flag[0]) issue(i + STAGES, policy_evict_last());
     }
   }
 
   if (threadIdx.x == 0) tl_stamp(tl, 7);
   fa_end<D>(fa);
   __syncthreads();  // the ring is free: every issued tile was consumed
-  {
+  if (KW > 1) {
+    // the second key group hands its (output, max, sum) to the first through the free ring;
+    // the first rescales both to the larger max and adds them
+    float4* s_o = reinterpret_cast<float4*>(smem);
+    float4* s_ml = s_o + nw * NT_D * 32;
+    if (kg == 1) {
+#pragma unroll
+      for (int nt = 0; nt < NT_D; ++nt)
+        s_o[(warp * NT_D + nt) * 32 + lane] = make_float4(fa.o[nt][0], fa.o[nt][1], fa.o[nt][2], fa.o[nt][3]);
+      s_ml[warp * 32 + lane] = make_float4(fa.m[0], fa.m[1], fa.l[0], fa.l[1]);
+    }
+    __syncthreads();
+    if (kg == 0) {
+      const float4 ml = s_ml[warp * 32 + lane];
+      const float mb[2] = {ml.x, ml.y}, lb[2] = {ml.z, ml.w};
+      float ca[2], cb[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float M = fmaxf(fa.m[r], mb[r]);
+        ca[r] = fa.m[r] == -INFINITY ? 0.f : exp2f(fa.m[r] - M);
+        cb[r] = mb[r] == -INFINITY ? 0.f : exp2f(mb[r] - M);
+        fa.l[r] = fa.l[r] * ca[r] + lb[r] * cb[r];
+        fa.m[r] = M;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT_D; ++nt) {
+        const float4 ob = s_o[(warp * NT_D + nt) * 32 + lane];
+        fa.o[nt][0] = fa.o[nt][0] * ca[0] + ob.x * cb[0];
+        fa.o[nt][1] = fa.o[nt][1] * ca[0] + ob.y * cb[0];
+        fa.o[nt][2] = fa.o[nt][2] * ca[1] + ob.z * cb[1];
+        fa.o[nt][3] = fa.o[nt][3] * ca[1] + ob.w * cb[1];
+      }
+    }
+    __syncthreads();
+  }
+  if (kg == 0) {
     // stage this CTA's partial output and (max, sum) of every row in the ring, in one block
     // per merging CTA k: [rows of k: D floats each][rows of k: (max, sum, 0, 0)]
     const int ra = warp * 16 + r0, rb = ra + 8;
@@ -172,7 +220,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   fence_async_shared();  // the bulk copies below read the staged partials
   __syncthreads();
   cluster_wait();  // every CTA of the cluster has started and armed its merge barrier
-  if (warp == 0 && lane < S) {  // one bulk copy per merging CTA, each from its own lane
+  if (threadIdx.x < 32 && lane < S) {  // one bulk copy per merging CTA, each from its own lane
     const int k = lane, nk = rows_of(k);
     if (nk > 0) {
       const uint32_t bytes = static_cast<uint32_t>(nk * (D + 4) * 4);
@@ -239,7 +287,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   if (threadIdx.x == 0) tl_stamp(tl, 9);
   // the staged partials stay in place until the peers' copies have read them; every copy
   // into this CTA's memory has landed (its merge barrier completed) or this CTA merges none
-  if (warp == 0 && lane < S) bulk_wait_read();
+  if (threadIdx.x < 32 && lane < S) bulk_wait_read();
   if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
 }
 
@@ -267,7 +315,7 @@ int attn_set_attributes() {
 int attn_resident_clusters(int split) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, 1, 1);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = attn_smem_max(128);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -289,7 +337,7 @@ static int launch_d(const AttnParams& p, int batch, int split, cudaStream_t stre
   const int group = p.nq / p.nkv;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, p.nkv, batch);
-  cfg.blockDim = dim3(32 * group);
+  cfg.blockDim = dim3(32 * group * p.key_groups);
   cfg.dynamicSmemBytes = attn_smem(D, group, split);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -1,8 +1,8 @@
 // Flash-attention building blocks of the block-attention kernel (sm_103a).
 //
 // One warp owns 16 query rows (the block's slots for one query head) and walks key tiles
-// of 64 staged in shared memory by TMA: K and V as fp16, each in boxes of 64 keys x 64 dims
-// (128-byte rows, 128-byte swizzle). S = Q Kᵀ and O += P V run on the tensor cores as
+// (64 or 32 keys) staged in shared memory by TMA: K and V as fp16, each in boxes of NK keys x
+// 64 dims (128-byte rows, 128-byte swizzle). S = Q Kᵀ and O += P V run on the tensor cores as
 // mma.sync m16n8k16 with fp16 operands and fp32 accumulation, with an online softmax in
 // registers in log2 units. fp16 carries 11 significant bits, the same as TF32: the scores
 // are the step's most rounding-sensitive quantity (the attention output is a weighted mean
@@ -15,7 +15,7 @@
 
 namespace dfl {
 
-constexpr int kAttnKeys = 64;  // keys per tile
+constexpr int kAttnKeys = 64;  // keys per tile of the standalone kernel
 
 DEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -39,12 +39,13 @@ DEV uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte address of element (key, d) in an fp16 K or V tile: D/64 TMA boxes of 64 keys x 128
-// bytes, each written with the 128-byte swizzle (16-byte chunk c of row r lands at chunk
-// c ^ (r & 7)).
+// Byte address of element (key, d) in an fp16 K or V tile of NK keys: D/64 TMA boxes of NK
+// keys x 128 bytes, each written with the 128-byte swizzle (16-byte chunk c of row r lands at
+// chunk c ^ (r & 7)).
+template <int NK>
 DEV uint32_t kv_addr(uint32_t base, int key, int d) {
   const int box = d >> 6, dd = d & 63;
-  return base + box * (kAttnKeys * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
+  return base + box * (NK * 128) + key * 128 + ((((dd >> 3) ^ (key & 7))) << 4);
 }
 
 template <int D>
@@ -76,27 +77,28 @@ DEV void fa_begin(FaState<D>& st, const __half* q, size_t row0, size_t ld, int h
   for (int i = 0; i < D / 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
 }
 
-// One tile of 64 keys starting at key0 (keys >= nkeys are masked out); kb / vb are the
-// shared-memory addresses of the staged fp16 K and V tiles.
-template <int D>
+// One tile of NK keys (64 or 32) starting at key0 (keys >= nkeys are masked out); kb / vb
+// are the shared-memory addresses of the staged fp16 K and V tiles.
+template <int D, int NK = kAttnKeys>
 DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, float scale_log2, int lane) {
   constexpr int NT_D = D / 8;
+  constexpr int NJ = NK / 8;  // 8-key column tiles of the scores
   const int kq = (lane & 3) * 2;
-  float sc[8][4];
+  float sc[NJ][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+  for (int j = 0; j < NJ; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
   // S = Q Kᵀ. ldmatrix hands lane t row t/4, halves 2(t%4)..+1 of each 8 x 8 matrix: with
   // rows = keys and columns = 8 dims that is the B fragment (k = dims, n = keys). Matrices
   // 0..3: keys 0-7 dims lo, keys 0-7 dims hi, keys 8-15 dims lo, keys 8-15 dims hi.
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
+    for (int np = 0; np < NK / 16; ++np) {
       const int mi = lane >> 3;
       const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
       const int d = kk * 16 + (mi & 1) * 8;
       uint32_t b[4];
-      ldsm_x4(kv_addr(kb, key, d), b);
+      ldsm_x4(kv_addr<NK>(kb, key, d), b);
       mma_f16_16816(sc[2 * np], st.qa[kk], b[0], b[1]);
       mma_f16_16816(sc[2 * np + 1], st.qa[kk], b[2], b[3]);
     }
@@ -104,7 +106,7 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
   // scale to log2 units, mask keys past the end, online softmax
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < NJ; ++j) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int key = key0 + j * 8 + kq + (c & 1);
@@ -126,7 +128,7 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
   }
   float ls[2] = {0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < NJ; ++j) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const float p = exp2f(sc[j][c] - mx[c >> 1]);
@@ -145,7 +147,7 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
   }
   // O += P V
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
+  for (int kk = 0; kk < NK / 16; ++kk) {
     uint32_t pa[4];
     pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
     pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
@@ -157,7 +159,7 @@ DEV void fa_tile(FaState<D>& st, uint32_t kb, uint32_t vb, int key0, int nkeys, 
       const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
       const int d = dp * 16 + (mi >> 1) * 8;
       uint32_t b[4];
-      ldsm_x4_trans(kv_addr(vb, key, d), b);
+      ldsm_x4_trans(kv_addr<NK>(vb, key, d), b);
       mma_f16_16816(st.o[2 * dp], pa, b[0], b[1]);
       mma_f16_16816(st.o[2 * dp + 1], pa, b[2], b[3]);
     }

@@ -159,6 +159,7 @@ struct dflash_handle {
   int attn_split = 0;          // CTAs per attention cluster (0: from the SM count)
   unsigned long long wait_ns = kDefaultWaitLimitNs;  // limit of every wait inside a kernel
   int attn_wide = 0;           // clusters of 12 the device holds at once (0: none)
+  int attn_key_groups = 2;     // warps per query head in the attention kernel (taking alternate tiles)
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -660,6 +661,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     A.tl = tl_take(h, static_cast<long long>(split) * c.n_kv_heads * batch);
     A.tl_id = h->tl_launch++;
     A.wait_ns = h->wait_ns;
+    A.key_groups = (c.n_heads / c.n_kv_heads <= 4) ? h->attn_key_groups : 1;
     if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
     note_launch(h, st);
     return DFLASH_OK;
@@ -800,6 +802,10 @@ int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
       if (value < 0 || value > 16) return DFLASH_E_INVAL;
       h->attn_split = static_cast<int>(value);
       return DFLASH_OK;
+    case DFLASH_OPT_ATTN_KEY_GROUPS:
+      if (value < 1 || value > 2) return DFLASH_E_INVAL;
+      h->attn_key_groups = static_cast<int>(value);
+      return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }
@@ -811,6 +817,7 @@ int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value) {
     case DFLASH_OPT_CHAIN_MAX: *value = h->chain_max; return DFLASH_OK;
     case DFLASH_OPT_GEMV_VARIANT: *value = h->gemv_pref; return DFLASH_OK;
     case DFLASH_OPT_ATTN_SPLIT: *value = h->attn_split; return DFLASH_OK;
+    case DFLASH_OPT_ATTN_KEY_GROUPS: *value = h->attn_key_groups; return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }

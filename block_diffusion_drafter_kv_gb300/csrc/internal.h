@@ -136,6 +136,7 @@ struct AttnParams {
   unsigned long long* tl;  // timeline records (kTlWords per CTA) or null
   int tl_id;
   unsigned long long wait_ns;  // limit of every wait in the kernel
+  int key_groups;          // 1, or 2 (GQA groups of at most 4 heads): warps taking alternate tiles
 };
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
 int attn_set_attributes();

@@ -204,11 +204,15 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
  *                             default 3 (4 k-boxes per stage, 2 stages)
  *   DFLASH_OPT_ATTN_SPLIT     CTAs per attention cluster, 0..16; 0 (default) chooses from
  *                             the SM count
+ *   DFLASH_OPT_ATTN_KEY_GROUPS  warps per query head in the attention kernel, 1..2; with 2
+ *                             (default; GQA groups of at most 4 heads) the two take
+ *                             alternate key tiles and are combined after the key loop
  * Values out of range return DFLASH_E_INVAL and leave the setting unchanged. */
 #define DFLASH_OPT_WAIT_LIMIT_NS 1
 #define DFLASH_OPT_CHAIN_MAX 2
 #define DFLASH_OPT_GEMV_VARIANT 3
 #define DFLASH_OPT_ATTN_SPLIT 4
+#define DFLASH_OPT_ATTN_KEY_GROUPS 5
 int dflash_set_option(dflash_handle* h, int32_t option, int64_t value);
 int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value);
 

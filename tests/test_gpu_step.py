@@ -125,6 +125,19 @@ def test_step_loop_matches_oracle(tiny, B):
     _step_loop(tiny, B)
 
 
+@pytest.mark.parametrize("B", [16, 4])
+def test_step_loop_with_one_key_group(tiny, B):
+    """The same loop with one warp per query head in the attention kernel (instead of two
+    taking alternate key tiles)."""
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    d = tiny.drafter
+    d.set_option(BND.OPT_ATTN_KEY_GROUPS, 1)
+    try:
+        _step_loop(tiny, B)
+    finally:
+        d.set_option(BND.OPT_ATTN_KEY_GROUPS, 2)
+
+
 def _step_loop(tiny, B):
     from gpu_util import check_draft, max_rel, LAYER_RTOL
     s, w = tiny.s, W_TINY
