@@ -134,6 +134,33 @@ def verify_greedy(target_logits: np.ndarray, drafted: np.ndarray) -> VerifyResul
     return VerifyResult(j + 1, g[: j + 1].astype(np.int64), int(g[j]), g.astype(np.int64))
 
 
+# ----------------------------------------------------------------------------- fused target verify
+
+def target_logits_from_hidden(hidden_bits: np.ndarray, gain_bits: np.ndarray, lm_bits: np.ndarray,
+                              eps: float, dtype=np.float64, chunk: int = 16384) -> np.ndarray:
+    """The target's logits of B block positions from its last hidden states: the target's
+    own final RMSNorm (gain g, the drafter's eps) and LM head, z = RMSNorm(h)·g · W_lmᵀ.
+    hidden [B, Ht], gain [Ht], lm [V, Ht] as bf16 bit patterns; returns [B, V]. The LM head
+    rows are widened `chunk` at a time; each logit is one whole dot product."""
+    h = rms_norm(bf16_to_float(hidden_bits, dtype), bf16_to_float(gain_bits, dtype), eps)
+    V = lm_bits.shape[0]
+    z = np.empty((h.shape[0], V), dtype=dtype)
+    for v0 in range(0, V, chunk):
+        z[:, v0:v0 + chunk] = h @ bf16_to_float(lm_bits[v0:v0 + chunk], dtype).T
+    return z
+
+
+def verify_greedy_from_hidden(hidden_bits: np.ndarray, gain_bits: np.ndarray, lm_bits: np.ndarray,
+                              drafted: np.ndarray, eps: float):
+    """Greedy verification starting from the target's last hidden states instead of its
+    logits (the target checks the drafted block in one parallel pass and keeps the longest
+    valid prefix: bpdata.com, introduction). The target's argmax g_i of each position comes
+    from its final norm and LM head (target_logits_from_hidden); the accept rule is
+    verify_greedy's. Returns (VerifyResult, logits [B, V])."""
+    z = target_logits_from_hidden(hidden_bits, gain_bits, lm_bits, eps)
+    return verify_greedy(z, drafted), z
+
+
 # ----------------------------------------------------------------------------- model
 
 @dataclass

@@ -152,3 +152,28 @@ def naive_verify(target_logits: np.ndarray, drafted: Sequence[int]):
         if all(int(drafted[i - 1]) == g[i - 1] for i in range(1, cand)):
             tau = cand
     return tau, g[:tau]
+
+
+def naive_verify_from_hidden(hidden_bits: np.ndarray, gain_bits: np.ndarray, lm_bits: np.ndarray,
+                             drafted: Sequence[int], eps: float):
+    """The target's greedy tokens from its last hidden states with scalar loops (norm, one
+    dot product per vocabulary row, a running argmax that keeps the first maximum), then
+    the try-every-tau acceptance. Returns (tau, committed, g)."""
+    g_w = _f(gain_bits)
+    W = _f(lm_bits)
+    g = []
+    for row in _f(hidden_bits):
+        a = _rmsnorm(list(row), g_w, eps)
+        best, arg = -math.inf, -1
+        for v in range(W.shape[0]):
+            z = float(np.dot(W[v], a))
+            if z > best:
+                best, arg = z, v
+        g.append(arg)
+    B = len(g)
+    tau = 1
+    for t in range(B, 0, -1):
+        if all(int(drafted[i]) == g[i] for i in range(t - 1)):
+            tau = t
+            break
+    return tau, g[:tau], g

@@ -7,6 +7,7 @@ import pytest
 import oracle.dflash_ref as R
 import test_oracle_math as M
 import test_oracle_model as MM
+import test_oracle_target_verify as TV
 import test_oracle_verify as V
 from golden_io import load_verify_cases
 
@@ -139,6 +140,17 @@ def _embed_row_next(self, tok):   # the uncached lookup widens the row after the
     return R.bf16_to_float(self.bits["embed"][(tok + 1) % self.s.vocab], self.dtype)
 
 
+def _target_no_final_norm(hidden_bits, gain_bits, lm_bits, eps, dtype=np.float64, chunk=16384):
+    h = R.bf16_to_float(hidden_bits, dtype) * R.bf16_to_float(gain_bits, dtype)
+    return h @ R.bf16_to_float(lm_bits, dtype).T
+
+
+def _target_no_gain(hidden_bits, gain_bits, lm_bits, eps, dtype=np.float64, chunk=16384):
+    h = R.bf16_to_float(hidden_bits, dtype)
+    h = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
+    return h @ R.bf16_to_float(lm_bits, dtype).T
+
+
 MUTATIONS = {
     "rope_sign": ("apply_rope", _rope_wrong_sign),
     "rope_interleaved_pairs": ("apply_rope", _rope_interleaved),
@@ -156,6 +168,8 @@ MUTATIONS = {
     "fc_missing_rmsnorm": ("Oracle.context_feature", _ctx_no_norm),
     "lm_chunk_bound_short": ("Oracle._lm_head", _lm_chunk_short),
     "uncached_embed_wrong_row": ("Oracle._embed_row", _embed_row_next),
+    "target_no_final_norm": ("target_logits_from_hidden", _target_no_final_norm),
+    "target_no_gain": ("target_logits_from_hidden", _target_no_gain),
 }
 
 
@@ -178,6 +192,9 @@ def _all_pins(tiny):
         "draft_naive": lambda: MM.test_draft_steps_match_naive_recomputation(tiny),
         "uncached_naive": lambda: MM.test_uncached_chunked_oracle_matches_naive(tiny),
         "uncached_equals_cached": lambda: MM.test_uncached_chunked_oracle_equals_cached(tiny),
+        "target_naive": lambda: [TV.test_matches_naive_scalar_loops(sd, b) for sd, b in ((0, 4), (2, 7))],
+        "target_planted": TV.test_planted_agreement_and_slot0_mismatch,
+        "target_scale": TV.test_final_norm_makes_logits_scale_invariant,
     }
     for name, fn in checks.items():
         try:
