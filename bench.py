@@ -584,6 +584,38 @@ def run_cuda(a):
         del gB
     log("[bench] draft by block: " + json.dumps({k: round(v * 1e3, 1) for k, v in draft_by_block.items()}))
 
+    # ---------------------------------------------------------------- fused target-side verify
+    # dflash_verify_greedy_hidden on a synthetic target head of this workload's size (final
+    # norm gain 1 + N(0, 0.1), LM head N(0, 0.02) [V][Ht] bf16, hidden states N(0, 1)): the
+    # target's norm, LM head and argmax of every block position, then the acceptance.
+    fused = None
+    if s.target_hidden <= 8192:
+        gt = torch.Generator(device="cuda").manual_seed(a.seed + 99)
+        t_gain = (1.0 + 0.1 * torch.randn(s.target_hidden, generator=gt, device="cuda")).to(torch.bfloat16)
+        t_lm = (0.02 * torch.randn(s.vocab, s.target_hidden, generator=gt, device="cuda")).to(torch.bfloat16)
+        t_hid = torch.randn(batch * B, s.target_hidden, generator=gt, device="cuda").to(torch.bfloat16)
+        g_fv = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fv, stream=stream):
+            dr.verify_hidden(t_hid, t_gain, t_lm, drafted, batch, B, accept, committed)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_fv.replay()
+            d0.record(stream)
+            for _ in range(n_draft):
+                g_fv.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        fv_ms = d0.elapsed_time(d1) / n_draft
+        fv_bytes = 2 * s.vocab * s.target_hidden + 2 * batch * B * s.target_hidden
+        fused = {"us": fv_ms * 1e3, "bytes": fv_bytes, "achieved_gbs": fv_bytes / (fv_ms * 1e-3) / 1e9,
+                 "frac_of_hbm": fv_bytes / (fv_ms * 1e-3) / 1e9 / float(peaks()[0]["hbm_gbs"]),
+                 "what": "dflash_verify_greedy_hidden: target final norm + LM head + argmax + acceptance"}
+        del g_fv, t_lm
+        log(f"[bench] fused target verify: {fv_ms * 1e3:.1f} us")
+        with torch.cuda.stream(stream):
+            reset()
+        stream.synchronize()
+
     # ---------------------------------------------------------------- traced pass (per-kernel)
     kern = {}
     roof = None
@@ -734,7 +766,7 @@ def run_cuda(a):
             "config": workload_config(w, ws, a.seed),
             "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
             "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
-            "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block,
+            "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block, "fused_target_verify": fused,
             "draft_flatness": (max(draft_by_block.values()) / min(draft_by_block.values())) if draft_by_block else None,
             "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "dflash_draft_block": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dflash_verify_greedy": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
                                        c_void_p]),
+    "dflash_verify_greedy_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                              c_void_p, c_void_p, c_void_p]),
     "dflash_linear_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                                      c_void_p]),
     "dflash_read_device_error": (c_int32, [c_void_p, POINTER(c_int32), c_int32, c_void_p]),
@@ -167,6 +169,15 @@ class Drafter:
         check(self.L.dflash_verify_greedy(self.h, target_logits.data_ptr(), _ptr(drafted), batch, block,
                                           accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
               "dflash_verify_greedy")
+
+    def verify_hidden(self, target_hidden, target_gain, target_lm_head, drafted, batch: int, block: int, accept_len,
+                      committed, stream=None):
+        """Greedy verification from the target's last hidden states (bf16 [batch*B][Ht]), its
+        final-norm gain (bf16 [Ht]) and LM head (bf16 [V][Ht])."""
+        check(self.L.dflash_verify_greedy_hidden(self.h, target_hidden.data_ptr(), target_gain.data_ptr(),
+                                                 target_lm_head.data_ptr(), _ptr(drafted), batch, block,
+                                                 accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
+              "dflash_verify_greedy_hidden")
 
     # -- helpers -------------------------------------------------------------------------
     def linear(self, W, X, Y, stream=None):

@@ -29,6 +29,7 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 struct WsLayout {
   size_t err, tile_cnt, cta_cnt, seq_cnt, rope_cos, rope_sin, part, best_v, best_i;
   size_t ss_fc, ss_x, ss_emb, cfeat, x, xg, q, o, act, vpart_v, vpart_i, chain_bar;
+  size_t tgt_xg, tgt_ss, tgt_g;  // fused target-side verification
   size_t total;
   int R;          // draft rows allocated (multiple of 16)
   int max_tiles;  // tile counters
@@ -78,6 +79,9 @@ WsLayout layout_of(const dflash_config& c) {
   L.vpart_v = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
   L.vpart_i = take(static_cast<size_t>(c.max_batch) * c.max_block * kMaxChunks * 4);
   L.chain_bar = take(static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4);
+  L.tgt_xg = take(2 * R * static_cast<size_t>(c.target_hidden) * 2);
+  L.tgt_ss = take(R * 4);
+  L.tgt_g = take(R * 4);
   L.total = off;
   return L;
 }
@@ -172,6 +176,7 @@ struct dflash_handle {
   uint8_t* ws = nullptr;
   WsLayout L{};
   CUtensorMap m_xg[4]{}, m_cfeat[4]{}, m_act[4]{}, m_o[4]{};  // by nb_index, over both planes
+  CUtensorMap m_txg[4]{};  // the target's normed-hidden operand (fused verification), by nb_index
   std::vector<CUtensorMap> m_kcache, m_vcache;
   int last_launches = 0;
   std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
@@ -375,7 +380,8 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
     ok = enc2d(&h->m_xg[k], h->ws + L.xg, H, 2 * L.R, box) &&
          enc2d(&h->m_cfeat[k], h->ws + L.cfeat, H, 2 * kMaxPassRows, box) &&
          enc2d(&h->m_act[k], h->ws + L.act, c.intermediate, 2 * L.R, box) &&
-         enc2d(&h->m_o[k], h->ws + L.o, c.n_heads * d, 2 * L.R, box);
+         enc2d(&h->m_o[k], h->ws + L.o, c.n_heads * d, 2 * L.R, box) &&
+         enc2d(&h->m_txg[k], h->ws + L.tgt_xg, c.target_hidden, 2 * L.R, box);
   }
   h->m_kcache.resize(c.n_layers);
   h->m_vcache.resize(c.n_layers);
@@ -718,6 +724,78 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   P.tl = tl_take(h, static_cast<long long>(P.chunks) * block * batch);
   P.tl_id = h->tl_launch++;
   if (launch_verify(P, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+  note_launch(h, st);
+  return DFLASH_OK;
+}
+
+int dflash_verify_greedy_hidden(dflash_handle* h, const void* target_hidden, const void* target_gain,
+                                const void* target_lm_head, const int32_t* drafted, int32_t batch, int32_t block,
+                                int32_t* accept_len, int32_t* committed, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  if (!target_hidden || !target_gain || !target_lm_head || !accept_len || !committed || batch < 1 || block < 1 ||
+      (block > 1 && !drafted))
+    return DFLASH_E_INVAL;
+  if (!aligned16(target_hidden) || !aligned16(target_gain) || !aligned16(target_lm_head) || !aligned4(drafted) ||
+      !aligned4(accept_len) || !aligned4(committed))
+    return DFLASH_E_INVAL;
+  if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
+  if (c.target_hidden > 8192) return DFLASH_E_CONFIG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  call_begin(h, st);
+  const int rows = batch * block, Ht = c.target_hidden, R = h->L.R;
+  CUtensorMap m_lm;
+  if (!enc2d(&m_lm, target_lm_head, Ht, c.vocab, 64)) return DFLASH_E_CUDA;
+  TargetPrepParams T{};
+  T.hidden = static_cast<const __nv_bfloat16*>(target_hidden);
+  T.gain = static_cast<const __nv_bfloat16*>(target_gain);
+  T.xg = h->at<__nv_bfloat16>(h->L.tgt_xg);
+  T.xg_lo = R;
+  T.ss = h->at<float>(h->L.tgt_ss);
+  T.Ht = Ht;
+  if (launch_target_prep(T, rows, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+  note_launch(h, st);
+  for (int row0 = 0; row0 < rows; row0 += kMaxPassRows) {  // the target's argmax of every row
+    const int nb = nb_for_rows(std::min(kMaxPassRows, rows - row0));
+    GemvParams P{};
+    gemv_common(h, P);
+    P.amap[0] = m_lm;
+    P.n_amaps = 1;
+    P.T = ceil_div(c.vocab, 128);
+    P.tile_start[1] = P.T;
+    P.KB = Ht / 64;
+    P.bmap = h->m_txg[nb_index(nb)];
+    P.b_row0 = row0;
+    P.b_lo = R;
+    P.grow0 = row0;
+    P.out_row0 = row0;
+    P.n_valid = rows;
+    P.op = OP_LMHEAD;
+    P.ss_in = h->at<float>(h->L.tgt_ss);
+    P.ss_parts = 1;
+    P.ss_stride = R;
+    P.ss_row0 = row0;
+    P.H = Ht;
+    P.rows_per_seq = block;
+    P.batch = batch;
+    P.vocab = c.vocab;
+    P.n_out = c.vocab;
+    P.best_v = h->at<float>(h->L.best_v);
+    P.best_i = h->at<int>(h->L.best_i);
+    P.drafted = h->at<int>(h->L.tgt_g);
+    P.lm_all_rows = 1;
+    DFL_TRY(run_gemv(h, P, nb, st));
+  }
+  AcceptParams A{};
+  A.g = h->at<int>(h->L.tgt_g);
+  A.drafted = drafted;
+  A.accept_len = accept_len;
+  A.committed = committed;
+  A.last_token = h->last_token;
+  A.batch = batch;
+  A.B = block;
+  if (launch_accept(A, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
   note_launch(h, st);
   return DFLASH_OK;
 }

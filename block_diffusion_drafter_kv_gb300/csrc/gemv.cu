@@ -877,7 +877,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               const int gr = P.grow0 + r;
               if (lane8 == 0 && gr < P.n_valid) {
                 const int s = gr / B, i = gr - s * B;
-                if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
+                if (P.lm_all_rows) P.drafted[gr] = bi;
+                else if (i >= 1) P.drafted[s * (B - 1) + i - 1] = bi;
               }
             }
           } else {

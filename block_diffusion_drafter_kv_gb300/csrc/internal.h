@@ -87,7 +87,8 @@ struct GemvParams {
   int vocab;
   float* best_v;            // [kMaxCtas][kMaxPassRows]
   int* best_i;
-  int* drafted;
+  int* drafted;             // drafts d_1..d_{B-1} of every sequence; with lm_all_rows, argmax of every row
+  int lm_all_rows;          // the target's greedy tokens: every row's argmax, at its row index
 };
 
 // Up to kMaxPhases projections run back to back in one persistent launch: phase p+1 may
@@ -176,6 +177,29 @@ struct VerifyParams {
   int tl_id;
 };
 int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pdl);
+
+// Fused target-side verification: rows of the target's last hidden states -> the bf16
+// planes of h * g (the LM head's operand) and each row's sum of squares; then, once the
+// row argmaxes g are known, the longest-prefix acceptance.
+struct TargetPrepParams {
+  const __nv_bfloat16* hidden;  // [rows][Ht]
+  const __nv_bfloat16* gain;    // [Ht]
+  __nv_bfloat16* xg;            // [rows][Ht] high plane; low plane xg_lo rows further on
+  int xg_lo;
+  float* ss;                    // [rows]
+  int Ht;
+};
+int launch_target_prep(const TargetPrepParams& p, int rows, cudaStream_t stream, bool pdl);
+
+struct AcceptParams {
+  const int* g;         // [batch][B] the target's greedy tokens
+  const int* drafted;   // [batch][B-1]
+  int* accept_len;
+  int* committed;
+  int* last_token;
+  int batch, B;
+};
+int launch_accept(const AcceptParams& p, cudaStream_t stream, bool pdl);
 
 int launch_plant(float* logits, const int* drafted, const uint8_t* masks, int n_steps, const int* step,
                  int batch, int B, int V, float bump, int* saved, cudaStream_t stream);

@@ -220,6 +220,101 @@ int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pd
   return static_cast<int>(cudaLaunchKernelEx(&cfg, verify_kernel, p));
 }
 
+// ---------------------------------------------------------------- fused target-side verification
+// The target's final RMSNorm folded into its LM head, as for the drafter's: the operand is
+// h * g as two bf16 planes (high, and the bf16 of the remainder) and the LM-head epilogue
+// scales each row by 1 / rms(h) from the sum of squares written here. All loads of a
+// thread are issued before its stores.
+__global__ void __launch_bounds__(256) target_prep_kernel(const TargetPrepParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int kMaxIter = 4;  // Ht <= 4 * 8 * blockDim
+  const int row = blockIdx.x;
+  const __nv_bfloat16* src = P.hidden + static_cast<size_t>(row) * P.Ht;
+  uint4 xs[kMaxIter], gs[kMaxIter];
+#pragma unroll
+  for (int it = 0; it < kMaxIter; ++it) {
+    const int f0 = (it * blockDim.x + threadIdx.x) * 8;
+    if (f0 < P.Ht) {
+      xs[it] = *reinterpret_cast<const uint4*>(src + f0);
+      gs[it] = *reinterpret_cast<const uint4*>(P.gain + f0);
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int it = 0; it < kMaxIter; ++it) {
+    const int f0 = (it * blockDim.x + threadIdx.x) * 8;
+    if (f0 >= P.Ht) continue;
+    const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(&xs[it]);
+    const __nv_bfloat16* gv = reinterpret_cast<const __nv_bfloat16*>(&gs[it]);
+    __nv_bfloat16 hi[8], lo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float x = __bfloat162float(xv[k]);
+      const float y = x * __bfloat162float(gv[k]);
+      hi[k] = __float2bfloat16_rn(y);
+      lo[k] = __float2bfloat16_rn(y - __bfloat162float(hi[k]));
+      ss += x * x;
+    }
+    const size_t off = static_cast<size_t>(row) * P.Ht + f0;
+    *reinterpret_cast<uint4*>(P.xg + off) = *reinterpret_cast<const uint4*>(hi);
+    *reinterpret_cast<uint4*>(P.xg + off + static_cast<size_t>(P.xg_lo) * P.Ht) = *reinterpret_cast<const uint4*>(lo);
+  }
+  __shared__ float red[8];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_down_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    P.ss[row] = t;
+  }
+}
+
+int launch_target_prep(const TargetPrepParams& p, int rows, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, target_prep_kernel, p));
+}
+
+// The longest prefix of drafts equal to the target's greedy tokens, plus the bonus token
+// (bpdata.com, introduction): one thread per sequence.
+__global__ void accept_kernel(const AcceptParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= P.batch) return;
+  const int B = P.B;
+  const int* g = P.g + static_cast<size_t>(s) * B;
+  int j = 0;
+  while (j < B - 1 && __ldcg(P.drafted + s * (B - 1) + j) == __ldcg(g + j)) ++j;
+  const int tau = j + 1;
+  P.accept_len[s] = tau;
+  P.last_token[s] = __ldcg(g + j);
+  for (int k = 0; k < B; ++k) P.committed[s * B + k] = k < tau ? __ldcg(g + k) : -1;
+}
+
+int launch_accept(const AcceptParams& p, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.batch + 127) / 128);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, accept_kernel, p));
+}
+
 // ---------------------------------------------------------------- synthetic target (harness)
 __global__ void plant_kernel(float* logits, const int* drafted, const uint8_t* masks, int n_steps,
                              const int* step, int batch, int B, int V, float bump, int* saved) {

@@ -181,6 +181,22 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
                          int32_t batch, int32_t block, int32_t* accept_len, int32_t* committed,
                          void* stream);
 
+/* Greedy verification starting from the target's last hidden states (bpdata.com DFlash
+ * article, introduction: the target checks the whole drafted block in one parallel pass and
+ * keeps the longest valid prefix). Fuses the target's own final RMSNorm (gain target_gain,
+ * the drafter's rms_eps), its LM head and the argmax of every block position into the
+ * library's weight-streaming kernels, then applies the acceptance rule of
+ * dflash_verify_greedy, so the [batch][B][V] fp32 logits never exist.
+ *   target_hidden   bf16 [batch * B][Ht] (Ht = target_hidden of the config, <= 8192):
+ *                   the target's last-layer hidden state at each block position
+ *   target_gain     bf16 [Ht] the target's final RMSNorm gain
+ *   target_lm_head  bf16 [V][Ht] the target's LM head (V = vocab of the config)
+ *   drafted, accept_len, committed: as for dflash_verify_greedy; last_token[s] is written.
+ * Pointers 16-byte aligned (token arrays 4-byte); ties go to the lowest index. */
+int dflash_verify_greedy_hidden(dflash_handle* h, const void* target_hidden, const void* target_gain,
+                                const void* target_lm_head, const int32_t* drafted, int32_t batch, int32_t block,
+                                int32_t* accept_len, int32_t* committed, void* stream);
+
 /* Weight-streaming bf16 GEMM of the draft path, exposed for testing the engine alone:
  * Y[r][m] = sum_k X[r][k] * W[m][k] in fp32 accumulation.
  *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (any rows; passes of 128),
