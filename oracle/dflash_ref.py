@@ -161,6 +161,49 @@ def verify_greedy_from_hidden(hidden_bits: np.ndarray, gain_bits: np.ndarray, lm
     return verify_greedy(z, drafted), z
 
 
+# ----------------------------------------------------------------------------- sampling verify
+
+@dataclass
+class SampleResult:
+    accept_len: int            # tau in [1, B]: accepted drafts plus the sampled token
+    committed: np.ndarray      # [tau] d_1..d_{tau-1}, then the sampled token
+    last_token: int            # committed[-1], the next block's slot 0
+    stop_row: int              # the row the last token was sampled from (tau - 1)
+
+
+def verify_sampling(target_logits: np.ndarray, drafted: np.ndarray, temperature: float,
+                    uniforms: np.ndarray) -> SampleResult:
+    """Verification when the target samples at a temperature (7minutos.es, "Casos de uso con
+    ejemplos": the method is also measured under sampling, at about 3.9x). The pages state no
+    accept rule; the reading taken here is the standard speculative-sampling rule for a
+    drafter whose proposal is its own argmax (a point mass q_i at d_{i+1}), which keeps the
+    committed tokens distributed exactly as the target's own samples:
+
+      p_i = softmax(target_logits[i] / temperature)
+      for i = 0..B-2: accept d_{i+1} if uniforms[i] < p_i(d_{i+1}) (= min(1, p_i / q_i));
+                      else stop at row i
+      at the stop row j the last token is sampled with uniforms[B-1] by inverse CDF (the
+      first index whose cumulative probability exceeds it) from
+        p_j without d_{j+1}, renormalised (the residual max(0, p_j - q_j)),  j < B-1
+        p_{B-1} itself (every draft accepted: the bonus token),             j = B-1
+
+    target_logits [B, V]; drafted [B-1]; uniforms [B] in [0, 1)."""
+    z = np.asarray(target_logits, dtype=np.float64) / float(temperature)
+    p = softmax(z, axis=-1)
+    B = p.shape[0]
+    j = 0
+    while j < B - 1 and float(uniforms[j]) < p[j, int(drafted[j])]:
+        j += 1
+    r = p[j].copy()
+    if j < B - 1:
+        r[int(drafted[j])] = 0.0
+    r /= r.sum()
+    tok = int(np.searchsorted(np.cumsum(r), float(uniforms[B - 1]), side="right"))
+    tok = min(tok, int(np.flatnonzero(r > 0)[-1]))
+    committed = np.array([int(t) for t in drafted[:j]] + [tok], dtype=np.int64)
+    return SampleResult(j + 1, committed, tok, j)
+
+
 # ----------------------------------------------------------------------------- model
 
 @dataclass

@@ -7,9 +7,10 @@ import pytest
 import oracle.dflash_ref as R
 import test_oracle_math as M
 import test_oracle_model as MM
+import test_oracle_sampling as SV
 import test_oracle_target_verify as TV
 import test_oracle_verify as V
-from golden_io import load_verify_cases
+from golden_io import load_sampling_cases, load_verify_cases
 
 
 def _rope_wrong_sign(x, pos, theta):
@@ -151,6 +152,34 @@ def _target_no_gain(hidden_bits, gain_bits, lm_bits, eps, dtype=np.float64, chun
     return h @ R.bf16_to_float(lm_bits, dtype).T
 
 
+_orig_sampling = R.verify_sampling
+
+
+def _sampling_keeps_draft(target_logits, drafted, temperature, uniforms):
+    # the residual keeps the rejected draft's probability
+    p = R.softmax(np.asarray(target_logits, np.float64) / temperature, axis=-1)
+    B = p.shape[0]
+    j = 0
+    while j < B - 1 and float(uniforms[j]) < p[j, int(drafted[j])]:
+        j += 1
+    tok = int(np.searchsorted(np.cumsum(p[j]), float(uniforms[B - 1]), side="right"))
+    return R.SampleResult(j + 1, np.array([int(t) for t in drafted[:j]] + [tok]), tok, j)
+
+
+def _sampling_no_temperature(target_logits, drafted, temperature, uniforms):
+    return _orig_sampling(target_logits, drafted, 1.0, uniforms)
+
+
+def _sampling_bonus_prev_row(target_logits, drafted, temperature, uniforms):
+    r = _orig_sampling(target_logits, drafted, temperature, uniforms)
+    B = np.asarray(target_logits).shape[0]
+    if r.accept_len < B:
+        return r
+    p = R.softmax(np.asarray(target_logits, np.float64)[B - 2] / temperature)
+    tok = int(np.searchsorted(np.cumsum(p), float(uniforms[B - 1]), side="right"))
+    return R.SampleResult(B, np.array(list(r.committed[:-1]) + [tok]), tok, B - 1)
+
+
 MUTATIONS = {
     "rope_sign": ("apply_rope", _rope_wrong_sign),
     "rope_interleaved_pairs": ("apply_rope", _rope_interleaved),
@@ -170,6 +199,9 @@ MUTATIONS = {
     "uncached_embed_wrong_row": ("Oracle._embed_row", _embed_row_next),
     "target_no_final_norm": ("target_logits_from_hidden", _target_no_final_norm),
     "target_no_gain": ("target_logits_from_hidden", _target_no_gain),
+    "sampling_residual_keeps_draft": ("verify_sampling", _sampling_keeps_draft),
+    "sampling_ignores_temperature": ("verify_sampling", _sampling_no_temperature),
+    "sampling_bonus_previous_row": ("verify_sampling", _sampling_bonus_prev_row),
 }
 
 
@@ -195,6 +227,9 @@ def _all_pins(tiny):
         "target_naive": lambda: [TV.test_matches_naive_scalar_loops(sd, b) for sd, b in ((0, 4), (2, 7))],
         "target_planted": TV.test_planted_agreement_and_slot0_mismatch,
         "target_scale": TV.test_final_norm_makes_logits_scale_invariant,
+        "sampling_golden": lambda: [SV.test_hand_worked_cases(c) for c in load_sampling_cases()],
+        "sampling_distribution": SV.test_committed_tokens_follow_the_target_distribution,
+        "sampling_low_temperature": SV.test_low_temperature_equals_greedy,
     }
     for name, fn in checks.items():
         try:
