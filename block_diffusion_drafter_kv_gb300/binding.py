@@ -48,6 +48,8 @@ SIGNATURES = {
     "dflash_draft_block": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dflash_verify_greedy": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
                                        c_void_p]),
+    "dflash_verify_sampling": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32, c_void_p,
+                                         c_void_p, c_void_p]),
     "dflash_verify_greedy_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                               c_void_p, c_void_p, c_void_p]),
     "dflash_linear_bf16": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p,
@@ -169,6 +171,14 @@ class Drafter:
         check(self.L.dflash_verify_greedy(self.h, target_logits.data_ptr(), _ptr(drafted), batch, block,
                                           accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
               "dflash_verify_greedy")
+
+    def verify_sampling(self, target_logits, drafted, uniforms, temperature: float, batch: int, block: int,
+                        accept_len, committed, stream=None):
+        """Speculative-sampling verification at `temperature` with caller-drawn uniforms
+        (fp32 [batch][B]: accept tests, then the sampling draw)."""
+        check(self.L.dflash_verify_sampling(self.h, target_logits.data_ptr(), _ptr(drafted), uniforms.data_ptr(),
+                                            float(temperature), batch, block, accept_len.data_ptr(),
+                                            committed.data_ptr(), _stream(stream)), "dflash_verify_sampling")
 
     def verify_hidden(self, target_hidden, target_gain, target_lm_head, drafted, batch: int, block: int, accept_len,
                       committed, stream=None):

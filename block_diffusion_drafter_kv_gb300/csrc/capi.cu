@@ -728,6 +728,43 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
   return DFLASH_OK;
 }
 
+int dflash_verify_sampling(dflash_handle* h, const float* target_logits, const int32_t* drafted,
+                           const float* uniforms, float temperature, int32_t batch, int32_t block,
+                           int32_t* accept_len, int32_t* committed, void* stream) {
+  if (!h) return DFLASH_E_INVAL;
+  if (!h->bound) return DFLASH_E_STATE;
+  const auto& c = h->cfg;
+  if (!target_logits || !uniforms || !accept_len || !committed || batch < 1 || block < 1 || (block > 1 && !drafted))
+    return DFLASH_E_INVAL;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return DFLASH_E_INVAL;
+  if (!aligned4(target_logits) || !aligned4(uniforms) || !aligned4(drafted) || !aligned4(accept_len) ||
+      !aligned4(committed))
+    return DFLASH_E_INVAL;
+  if (batch > c.max_batch || block > c.max_block) return DFLASH_E_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  call_begin(h, st);
+  VerifySampleParams P{};
+  P.logits = target_logits;
+  P.drafted = drafted;
+  P.uniforms = uniforms;
+  P.inv_temp = 1.f / temperature;
+  P.accept_len = accept_len;
+  P.committed = committed;
+  P.last_token = h->last_token;
+  P.part_m = h->at<float>(h->L.vpart_v);
+  P.part_s = h->at<float>(h->L.vpart_i);
+  P.seq_cnt = h->at<int>(h->L.seq_cnt);
+  P.err = h->at<int>(h->L.err);
+  P.B = block;
+  P.V = c.vocab;
+  const int chunks = std::max(1, std::min(kMaxChunks, ceil_div(2LL * h->n_sms, static_cast<long long>(batch) * block)));
+  P.chunk_len = static_cast<int>(align_up(static_cast<size_t>(ceil_div(c.vocab, chunks)), 1024));
+  P.chunks = ceil_div(c.vocab, P.chunk_len);
+  if (launch_verify_sampling(P, batch, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+  note_launch(h, st);
+  return DFLASH_OK;
+}
+
 int dflash_verify_greedy_hidden(dflash_handle* h, const void* target_hidden, const void* target_gain,
                                 const void* target_lm_head, const int32_t* drafted, int32_t batch, int32_t block,
                                 int32_t* accept_len, int32_t* committed, void* stream) {

@@ -178,6 +178,25 @@ struct VerifyParams {
 };
 int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pdl);
 
+// Sampling-mode verification (temperature > 0): speculative sampling with the drafts as
+// point proposals. Same chunked grid as verify_kernel; the partials are per-chunk
+// (max, sum of exp) of z / T.
+struct VerifySampleParams {
+  const float* logits;    // [batch][B][V]
+  const int* drafted;     // [batch][B-1]
+  const float* uniforms;  // [batch][B]: accept tests u_0..u_{B-2}, then w for the sampled token
+  float inv_temp;
+  int* accept_len;
+  int* committed;
+  int* last_token;
+  float* part_m;          // [batch][B][chunks]
+  float* part_s;
+  int* seq_cnt;           // [batch]
+  int* err;
+  int B, V, chunks, chunk_len;
+};
+int launch_verify_sampling(const VerifySampleParams& p, int batch, cudaStream_t stream, bool pdl);
+
 // Fused target-side verification: rows of the target's last hidden states -> the bf16
 // planes of h * g (the LM head's operand) and each row's sum of squares; then, once the
 // row argmaxes g are known, the longest-prefix acceptance.

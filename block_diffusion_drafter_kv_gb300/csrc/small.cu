@@ -220,6 +220,200 @@ int launch_verify(const VerifyParams& p, int batch, cudaStream_t stream, bool pd
   return static_cast<int>(cudaLaunchKernelEx(&cfg, verify_kernel, p));
 }
 
+// ---------------------------------------------------------------- sampling-mode verification
+// Verification when the target samples at temperature T (7minutos.es, "Casos de uso con
+// ejemplos", measures the method under sampling). The pages give no accept rule; this is
+// standard speculative sampling with the drafter's argmax as a point proposal: accept
+// d_{i+1} while u_i < p_i(d_{i+1}), p_i = softmax(z_i / T); at the first rejection (row j)
+// sample by inverse CDF with w from p_j without d_{j+1}; with every draft accepted sample
+// the bonus token from p_{B-1}. The uniforms are inputs.
+//
+// Grid (chunks, B, batch): each CTA reduces one chunk of one row to (max, sum of exp) of
+// z / T; the last CTA of a sequence merges the chunks of every row, takes the accept
+// decisions, finds the chunk in which the cumulative mass of the stop row crosses
+// w * (its mass), and scans that chunk with a block-wide prefix sum.
+DEV void lse_merge(float& m, float& s, float om, float os) {
+  const float M = fmaxf(m, om);
+  if (M == -INFINITY) return;
+  s = (m == -INFINITY ? 0.f : s * __expf(m - M)) + (om == -INFINITY ? 0.f : os * __expf(om - M));
+  m = M;
+}
+
+__global__ void __launch_bounds__(256) verify_sampling_kernel(const VerifySampleParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int chunk = blockIdx.x, i = blockIdx.y, sq = blockIdx.z;
+  const int B = P.B, V = P.V, tid = threadIdx.x;
+  const float* row = P.logits + (static_cast<size_t>(sq) * B + i) * V;
+  const int c0 = chunk * P.chunk_len, c1 = min(V, c0 + P.chunk_len);
+  float m = -INFINITY, sum = 0.f;  // online max and sum of exp(z / T - max) over the chunk
+  for (int k = c0 + tid; k < c1; k += blockDim.x) {
+    const float t = __ldcg(row + k) * P.inv_temp;
+    if (t > m) {
+      sum = (m == -INFINITY ? 0.f : sum * __expf(m - t)) + 1.f;
+      m = t;
+    } else {
+      sum += __expf(t - m);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float om = __shfl_down_sync(0xffffffffu, m, o), os = __shfl_down_sync(0xffffffffu, sum, o);
+    lse_merge(m, sum, om, os);
+  }
+  __shared__ float wm[8], ws[8];
+  __shared__ int s_last;
+  if ((tid & 31) == 0) {
+    wm[tid >> 5] = m;
+    ws[tid >> 5] = sum;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) lse_merge(m, sum, wm[w], ws[w]);
+    const int slot = (sq * B + i) * P.chunks + chunk;
+    P.part_m[slot] = m;
+    P.part_s[slot] = sum;
+    __threadfence();
+    const int old = atomicAdd(P.seq_cnt + sq, 1);
+    s_last = (old == B * P.chunks - 1);
+    if (s_last) P.seq_cnt[sq] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // ---- last CTA of the sequence: every row's (max, sum), the accept decisions
+  __shared__ float rm[16], rs[16], pd[16];
+  __shared__ int s_j, s_tok, s_chunk, s_excl;
+  __shared__ float s_w, s_mj;
+  __shared__ float scan[256];
+  {
+    const int r = tid >> 4, l16 = tid & 15;
+    float mm = -INFINITY, ss = 0.f;
+    if (r < B)
+      for (int c = l16; c < P.chunks; c += 16) {
+        const int slot = (sq * B + r) * P.chunks + c;
+        lse_merge(mm, ss, __ldcg(P.part_m + slot), __ldcg(P.part_s + slot));
+      }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+      const float om = __shfl_down_sync(0xffffffffu, mm, o, 16), os = __shfl_down_sync(0xffffffffu, ss, o, 16);
+      lse_merge(mm, ss, om, os);
+    }
+    if (r < B && l16 == 0) {
+      rm[r] = mm;
+      rs[r] = ss;
+      float p = 0.f;
+      if (r < B - 1) {
+        const int d = __ldcg(P.drafted + sq * (B - 1) + r);
+        if (d >= 0 && d < V) {
+          p = __expf(__ldcg(P.logits + (static_cast<size_t>(sq) * B + r) * V + d) * P.inv_temp - mm) / ss;
+        } else {
+          raise_flag(P.err, kDevToken);
+        }
+      }
+      pd[r] = p;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const float* u = P.uniforms + static_cast<size_t>(sq) * B;
+    int j = 0;
+    while (j < B - 1 && __ldcg(u + j) < pd[j]) ++j;
+    const float* zj = P.logits + (static_cast<size_t>(sq) * B + j) * V;
+    const int excl = j < B - 1 ? __ldcg(P.drafted + sq * (B - 1) + j) : -1;
+    const float mj = rm[j];
+    const float e_ex = (excl >= 0 && excl < V) ? __expf(__ldcg(zj + excl) * P.inv_temp - mj) : 0.f;
+    float W = __ldcg(u + B - 1) * (rs[j] - e_ex);
+    // the chunk in which the cumulative mass of row j (without the rejected draft) passes W
+    float acc = 0.f;
+    int cs = P.chunks - 1;
+    float w_in = INFINITY;  // not crossed (rounding): the last index of the last chunk
+    for (int c = 0; c < P.chunks; ++c) {
+      const int slot = (sq * B + j) * P.chunks + c;
+      const float pm = __ldcg(P.part_m + slot);
+      float mc = pm == -INFINITY ? 0.f : __ldcg(P.part_s + slot) * __expf(pm - mj);
+      if (excl >= c * P.chunk_len && excl < (c + 1) * P.chunk_len) mc -= e_ex;
+      if (W < acc + mc) {
+        cs = c;
+        w_in = W - acc;
+        break;
+      }
+      acc += mc;
+    }
+    s_j = j;
+    s_excl = excl;
+    s_mj = mj;
+    s_chunk = cs;
+    s_w = w_in;
+    s_tok = -1;
+  }
+  __syncthreads();
+  // ---- block-wide scan of the chosen chunk of row j: each thread a contiguous segment
+  {
+    const int j = s_j, excl = s_excl, cs = max(s_chunk, 0);
+    const float mj = s_mj;
+    const float* zj = P.logits + (static_cast<size_t>(sq) * B + j) * V;
+    const int a0 = cs * P.chunk_len, a1 = min(V, a0 + P.chunk_len);
+    const int seg = (a1 - a0 + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(a1, a0 + tid * seg), b1 = min(a1, b0 + seg);
+    float local = 0.f;
+    for (int v = b0; v < b1; ++v)
+      if (v != excl) local += __expf(__ldcg(zj + v) * P.inv_temp - mj);
+    scan[tid] = local;
+    __syncthreads();
+    for (int o = 1; o < static_cast<int>(blockDim.x); o <<= 1) {  // inclusive prefix sums
+      const float add = tid >= o ? scan[tid - o] : 0.f;
+      __syncthreads();
+      scan[tid] += add;
+      __syncthreads();
+    }
+    const float before = scan[tid] - local, Wc = s_w;
+    if (Wc >= before && Wc < scan[tid]) {
+      float a = before;
+      int hit = -1, lastv = -1;
+      for (int v = b0; v < b1; ++v) {
+        if (v == excl) continue;
+        lastv = v;
+        a += __expf(__ldcg(zj + v) * P.inv_temp - mj);
+        if (Wc < a) {
+          hit = v;
+          break;
+        }
+      }
+      s_tok = hit >= 0 ? hit : lastv;  // rounding within the segment: its last index
+    }
+    __syncthreads();
+    if (tid == 0 && s_tok < 0) {  // rounding: the last index of the chunk that carries mass
+      for (int v = a1 - 1; v >= a0; --v)
+        if (v != excl) {
+          s_tok = v;
+          break;
+        }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int j = s_j, tok = s_tok;
+    P.accept_len[sq] = j + 1;
+    P.last_token[sq] = tok;
+    for (int k = 0; k < B; ++k)
+      P.committed[sq * B + k] = k < j ? __ldcg(P.drafted + sq * (B - 1) + k) : (k == j ? tok : -1);
+  }
+}
+
+int launch_verify_sampling(const VerifySampleParams& p, int batch, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.chunks, p.B, batch);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, verify_sampling_kernel, p));
+}
+
 // ---------------------------------------------------------------- fused target-side verification
 // The target's final RMSNorm folded into its LM head, as for the drafter's: the operand is
 // h * g as two bf16 planes (high, and the bf16 of the remainder) and the LM-head epilogue

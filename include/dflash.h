@@ -181,6 +181,28 @@ int dflash_verify_greedy(dflash_handle* h, const float* target_logits, const int
                          int32_t batch, int32_t block, int32_t* accept_len, int32_t* committed,
                          void* stream);
 
+/* Verification when the target samples at a temperature (7minutos.es, "Casos de uso con
+ * ejemplos": the method is also measured under sampling). The pages state no accept rule;
+ * this is standard speculative sampling with the drafter's argmax as a point proposal,
+ * which keeps the committed tokens distributed as the target's own samples:
+ *   p_i = softmax(target_logits[s][i] / temperature)
+ *   accept d_{i+1} (= drafted[s][i]) while u_i < p_i(d_{i+1}), i = 0..B-2;
+ *   at the first rejection (row j) the last token is sampled from p_j without d_{j+1},
+ *   renormalised; with every draft accepted it is the bonus token sampled from p_{B-1}.
+ *   The token is the first index whose cumulative probability exceeds w (inverse CDF).
+ *   target_logits  fp32 [batch][B][V], finite
+ *   drafted        int32 [batch][B-1]
+ *   uniforms       fp32 [batch][B] in [0, 1): u_0..u_{B-2}, then w (the caller's random
+ *                  numbers; the library draws none)
+ *   temperature    > 0
+ *   accept_len     int32 [batch] out: tau in [1, B] (accepted drafts plus the sampled token)
+ *   committed      int32 [batch][B] out: d_1..d_{tau-1}, the sampled token, then -1
+ * Writes last_token[s] = the sampled token. Sums run in fp32: where a uniform lies within
+ * about 1e-6 of a decision boundary the outcome may differ from an exact evaluation. */
+int dflash_verify_sampling(dflash_handle* h, const float* target_logits, const int32_t* drafted,
+                           const float* uniforms, float temperature, int32_t batch, int32_t block,
+                           int32_t* accept_len, int32_t* committed, void* stream);
+
 /* Greedy verification starting from the target's last hidden states (bpdata.com DFlash
  * article, introduction: the target checks the whole drafted block in one parallel pass and
  * keeps the longest valid prefix). Fuses the target's own final RMSNorm (gain target_gain,
