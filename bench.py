@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=30.0)
     ap.add_argument("--trace-steps", type=int, default=10)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the block-size draft sweep and the fused target-verify measurement")
     return ap.parse_args()
 
 
@@ -435,10 +437,31 @@ def run_cuda(a):
     hid_ctx = torch.empty(s.n_taps, batch * ctx_max, s.target_hidden, dtype=torch.bfloat16, device="cuda")
     hid_ctx.normal_(generator=torch.Generator(device="cuda").manual_seed(a.seed * 1000 + rank))
     n_ctx = torch.as_tensor(ctx_lens, dtype=torch.int32, device="cuda")
+    pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        pf0.record(stream)
         dr.inject(hid_ctx, ctx_max, n_ctx, batch)
+        pf1.record(stream)
         dr.last_token[:batch].copy_(torch.as_tensor(I.initial_tokens(batch, s.vocab, a.seed + rank)))
     stream.synchronize()
+    prefill = {"positions": int(ctx_lens.sum()), "pass_rows": dr.get_option(BND.OPT_INJECT_PASS_ROWS),
+               "us": 1e3 * pf0.elapsed_time(pf1)}
+    if not a.no_sweep and dr.get_option(BND.OPT_INJECT_PASS_ROWS) < 128:
+        # the same prefill through 128-row passes (a handle of its own: the width is fixed
+        # per handle), each pass streaming the fusion and K/V weights once
+        wide = BND.Drafter(s, weights, max_block=B, max_batch=batch, kv_capacity=cap)
+        wide.set_option(BND.OPT_INJECT_PASS_ROWS, 128)
+        with torch.cuda.stream(stream):
+            wide.inject(hid_ctx, ctx_max, n_ctx, batch)   # warm-up
+            wide.len.zero_()
+            pf0.record(stream)
+            wide.inject(hid_ctx, ctx_max, n_ctx, batch)
+            pf1.record(stream)
+        stream.synchronize()
+        prefill["us_128_row_passes"] = 1e3 * pf0.elapsed_time(pf1)
+        wide.close()
+        del wide
+    log(f"[bench] prefill: {json.dumps(prefill)}")
     del hid_ctx
     len0 = dr.len.clone()
     last0 = dr.last_token.clone()
@@ -563,7 +586,7 @@ def run_cuda(a):
     # the same for every block size of the sweep (the block rides in the N operand of every
     # weight stream, so the draft's cost should barely depend on it)
     draft_by_block = {}
-    for Bs in (4, 8, 12, 16):
+    for Bs in (() if a.no_sweep else (4, 8, 12, 16)):
         if Bs > B:
             continue
         if Bs == B:
@@ -589,7 +612,7 @@ def run_cuda(a):
     # norm gain 1 + N(0, 0.1), LM head N(0, 0.02) [V][Ht] bf16, hidden states N(0, 1)): the
     # target's norm, LM head and argmax of every block position, then the acceptance.
     fused = None
-    if s.target_hidden <= 8192:
+    if s.target_hidden <= 8192 and not a.no_sweep:
         gt = torch.Generator(device="cuda").manual_seed(a.seed + 99)
         t_gain = (1.0 + 0.1 * torch.randn(s.target_hidden, generator=gt, device="cuda")).to(torch.bfloat16)
         t_lm = (0.02 * torch.randn(s.vocab, s.target_hidden, generator=gt, device="cuda")).to(torch.bfloat16)
@@ -767,6 +790,7 @@ def run_cuda(a):
             "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
             "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
             "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block, "fused_target_verify": fused,
+            "prefill": prefill,
             "draft_flatness": (max(draft_by_block.values()) / min(draft_by_block.values())) if draft_by_block else None,
             "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,

@@ -19,6 +19,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: 
           -4: "CUDA error", -5: "state not bound"}
 DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4
 OPT_WAIT_LIMIT_NS, OPT_CHAIN_MAX, OPT_GEMV_VARIANT, OPT_ATTN_SPLIT, OPT_ATTN_KEY_GROUPS = 1, 2, 3, 4, 5
+OPT_INJECT_PASS_ROWS = 6
 
 
 class DflashConfig(ctypes.Structure):
@@ -44,6 +45,8 @@ SIGNATURES = {
     "dflash_create": (c_int32, [POINTER(DflashConfig), POINTER(DflashWeights), POINTER(c_void_p)]),
     "dflash_destroy": (c_int32, [c_void_p]),
     "dflash_bind_state": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t]),
+    "dflash_bind_state_paged": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p,
+                                          c_void_p, c_void_p, c_size_t]),
     "dflash_inject_ctx": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p]),
     "dflash_draft_block": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dflash_verify_greedy": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
@@ -123,7 +126,12 @@ class Drafter:
 
     `weights` has the attributes of the input generator's `Weights` (bf16 CUDA tensors)."""
 
-    def __init__(self, shape, weights, max_block: int, max_batch: int, kv_capacity: int):
+    def __init__(self, shape, weights, max_block: int, max_batch: int, kv_capacity: int, n_pages: int = 0,
+                 page_table=None):
+        """n_pages > 0 binds a paged KV cache: a pool of n_pages pages of 64 positions
+        (k_cache / v_cache [L][n_pages * 64][nkv][d]) and `page_table`, an int32 CUDA tensor
+        [max_batch][pages_per_seq] of page ids that the caller fills (and may change between
+        calls)."""
         import torch
         self.L = lib()
         self.shape = shape
@@ -142,10 +150,10 @@ class Drafter:
         self.h = h
         dev = weights.w_fc.device
         s = shape
-        self.k_cache = torch.zeros(s.n_layers, max_batch, kv_capacity, s.n_kv_heads, s.head_dim,
-                                   dtype=torch.float16, device=dev)
-        self.v_cache = torch.zeros(s.n_layers, max_batch, kv_capacity, s.n_kv_heads, s.head_dim,
-                                   dtype=torch.float16, device=dev)
+        rows = (n_pages * 64,) if n_pages else (max_batch, kv_capacity)
+        self.k_cache = torch.zeros(s.n_layers, *rows, s.n_kv_heads, s.head_dim, dtype=torch.float16, device=dev)
+        self.v_cache = torch.zeros(s.n_layers, *rows, s.n_kv_heads, s.head_dim, dtype=torch.float16, device=dev)
+        self.page_table = page_table
         self.len = torch.zeros(max_batch, dtype=torch.int32, device=dev)
         self.last_token = torch.zeros(max_batch, dtype=torch.int32, device=dev)
         nbytes = self.L.dflash_workspace_size(ctypes.byref(self.cfg))
@@ -154,9 +162,16 @@ class Drafter:
         self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
         base = self.workspace.data_ptr()
         self._ws_ptr = (base + 255) // 256 * 256
-        check(self.L.dflash_bind_state(self.h, self.k_cache.data_ptr(), self.v_cache.data_ptr(),
-                                       self.len.data_ptr(), self.last_token.data_ptr(), self._ws_ptr, nbytes),
-              "dflash_bind_state")
+        if n_pages:
+            assert page_table is not None and page_table.dtype == torch.int32 and page_table.is_cuda
+            check(self.L.dflash_bind_state_paged(self.h, self.k_cache.data_ptr(), self.v_cache.data_ptr(), n_pages,
+                                                 page_table.data_ptr(), page_table.shape[1], self.len.data_ptr(),
+                                                 self.last_token.data_ptr(), self._ws_ptr, nbytes),
+                  "dflash_bind_state_paged")
+        else:
+            check(self.L.dflash_bind_state(self.h, self.k_cache.data_ptr(), self.v_cache.data_ptr(),
+                                           self.len.data_ptr(), self.last_token.data_ptr(), self._ws_ptr, nbytes),
+                  "dflash_bind_state")
 
     # -- the three calls of the step ---------------------------------------------------
     def inject(self, hidden, rows_per_seq: int, n_new, batch: int, stream=None):

@@ -25,6 +25,7 @@ namespace dfl {
 namespace {
 
 constexpr int KT = kAttnKeys;  // keys per tile
+static_assert(KT == kPageRows, "a key tile is one page of a paged cache");
 constexpr int STAGES = 3;
 
 // Offset of the merge inputs from the 1024-aligned base: the ring of fp16 K + V tiles, its
@@ -105,7 +106,12 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
     const int st = i % STAGES;
     uint8_t* kd = smem + st * TILE_BYTES;
     uint8_t* vd = kd + K_BYTES;
-    const int row = key_row0 + (t0 + i) * KT;
+    int row = key_row0 + (t0 + i) * KT;
+    if (P.page_table) {  // tile t of a sequence is its page t
+      const int page = __ldcg(P.page_table + static_cast<size_t>(seq) * P.pages_per_seq + t0 + i);
+      if (page < 0 || page >= P.n_pages) raise_flag(P.err, kDevCapacity);
+      row = (page < 0 || page >= P.n_pages) ? 0 : page * KT;
+    }
     mbar_arrive_expect_tx(&full[st], TILE_BYTES);
 #pragma unroll
     for (int b = 0; b < D / 64; ++b) tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);

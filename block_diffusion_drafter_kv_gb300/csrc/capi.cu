@@ -171,6 +171,9 @@ struct dflash_handle {
   bool bound = false;
   __half* kc = nullptr;
   __half* vc = nullptr;
+  int layer_rows = 0;              // positions per layer of the cache
+  const int* page_table = nullptr; // paged cache: [max_batch][pages_per_seq], or null
+  int pages_per_seq = 0;
   int* len = nullptr;
   int* last_token = nullptr;
   uint8_t* ws = nullptr;
@@ -344,16 +347,23 @@ int dflash_destroy(dflash_handle* h) {
   return DFLASH_OK;
 }
 
-int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* len, int32_t* last_token,
-                      void* workspace, size_t workspace_bytes) {
-  if (!h || !k_cache || !v_cache || !len || !last_token || !workspace) return DFLASH_E_INVAL;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(k_cache) || !aligned16(v_cache))
-    return DFLASH_E_INVAL;
+}  // extern "C"
+
+namespace {
+
+// Shared by both binding calls: records the caches (sequence-major when page_table is null,
+// else a pool of layer_rows positions per layer in pages of kPageRows), fills the RoPE
+// tables, clears the workspace and encodes the tensor maps over caches and workspace.
+int bind_common(dflash_handle* h, void* k_cache, void* v_cache, int layer_rows, const int32_t* page_table,
+                int pages_per_seq, int32_t* len, int32_t* last_token, void* workspace, size_t workspace_bytes) {
   const auto& c = h->cfg;
   const WsLayout L = layout_of(c);
   if (workspace_bytes < L.total) return DFLASH_E_CAPACITY;
   h->kc = static_cast<__half*>(k_cache);
   h->vc = static_cast<__half*>(v_cache);
+  h->layer_rows = layer_rows;
+  h->page_table = page_table;
+  h->pages_per_seq = pages_per_seq;
   h->len = len;
   h->last_token = last_token;
   h->ws = static_cast<uint8_t*>(workspace);
@@ -385,15 +395,43 @@ int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* l
   }
   h->m_kcache.resize(c.n_layers);
   h->m_vcache.resize(c.n_layers);
-  const size_t layer_elems = static_cast<size_t>(c.max_batch) * c.kv_capacity * c.n_kv_heads * d;
+  const size_t layer_elems = static_cast<size_t>(layer_rows) * c.n_kv_heads * d;
   for (int l = 0; l < c.n_layers && ok; ++l) {
-    const uint64_t rows = static_cast<uint64_t>(c.max_batch) * c.kv_capacity;
-    ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, rows) &&
-         enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, rows);
+    ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, layer_rows) &&
+         enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, layer_rows);
   }
   if (!ok) return DFLASH_E_CUDA;
   h->bound = true;
   return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* len, int32_t* last_token,
+                      void* workspace, size_t workspace_bytes) {
+  if (!h || !k_cache || !v_cache || !len || !last_token || !workspace) return DFLASH_E_INVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(k_cache) || !aligned16(v_cache))
+    return DFLASH_E_INVAL;
+  const auto& c = h->cfg;
+  return bind_common(h, k_cache, v_cache, c.max_batch * c.kv_capacity, nullptr, 0, len, last_token, workspace,
+                     workspace_bytes);
+}
+
+int dflash_bind_state_paged(dflash_handle* h, void* k_pool, void* v_pool, int32_t n_pages,
+                            const int32_t* page_table, int32_t pages_per_seq, int32_t* len, int32_t* last_token,
+                            void* workspace, size_t workspace_bytes) {
+  if (!h || !k_pool || !v_pool || !page_table || !len || !last_token || !workspace) return DFLASH_E_INVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned4(page_table))
+    return DFLASH_E_INVAL;
+  const auto& c = h->cfg;
+  if (n_pages < 1 || pages_per_seq < 1 || static_cast<long long>(pages_per_seq) * kPageRows < c.kv_capacity ||
+      static_cast<long long>(n_pages) * kPageRows >= (1LL << 31))
+    return DFLASH_E_INVAL;
+  return bind_common(h, k_pool, v_pool, n_pages * kPageRows, page_table, pages_per_seq, len, last_token, workspace,
+                     workspace_bytes);
 }
 
 int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq, const int32_t* n_new,
@@ -465,8 +503,11 @@ int dflash_inject_ctx(dflash_handle* h, const void* hidden, int32_t rows_per_seq
       P.rope_cos = h->at<float>(h->L.rope_cos);
       P.rope_sin = h->at<float>(h->L.rope_sin);
       P.d = d;
-      P.kc = h->kc + static_cast<size_t>(l0) * c.max_batch * c.kv_capacity * c.n_kv_heads * d;
-      P.vc = h->vc + static_cast<size_t>(l0) * c.max_batch * c.kv_capacity * c.n_kv_heads * d;
+      P.kc = h->kc + static_cast<size_t>(l0) * h->layer_rows * c.n_kv_heads * d;
+      P.vc = h->vc + static_cast<size_t>(l0) * h->layer_rows * c.n_kv_heads * d;
+      P.layer_rows = h->layer_rows;
+      P.page_table = h->page_table;
+      P.pages_per_seq = h->pages_per_seq;
       P.nkv = c.n_kv_heads;
       P.cap = c.kv_capacity;
       P.max_batch = c.max_batch;
@@ -559,6 +600,9 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     P.d = d;
     P.kc = h->kc;
     P.vc = h->vc;
+    P.layer_rows = h->layer_rows;
+    P.page_table = h->page_table;
+    P.pages_per_seq = h->pages_per_seq;
     P.nkv = c.n_kv_heads;
     P.cap = c.kv_capacity;
     P.max_batch = c.max_batch;
@@ -650,6 +694,9 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     A.o = h->at<__nv_bfloat16>(h->L.o);
     A.o_lo = R;
     A.len = h->len;
+    A.page_table = h->page_table;
+    A.pages_per_seq = h->pages_per_seq;
+    A.n_pages = h->layer_rows / kPageRows;
     A.err = h->at<int>(h->L.err);
     A.B = block;
     A.nq = c.n_heads;
@@ -921,6 +968,10 @@ int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
       if (value < 1 || value > 2) return DFLASH_E_INVAL;
       h->attn_key_groups = static_cast<int>(value);
       return DFLASH_OK;
+    case DFLASH_OPT_INJECT_PASS_ROWS:
+      if (value != 16 && value != 32 && value != 64 && value != 128) return DFLASH_E_INVAL;
+      h->inject_pass_rows = static_cast<int>(value);
+      return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }
@@ -933,6 +984,7 @@ int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value) {
     case DFLASH_OPT_GEMV_VARIANT: *value = h->gemv_pref; return DFLASH_OK;
     case DFLASH_OPT_ATTN_SPLIT: *value = h->attn_split; return DFLASH_OK;
     case DFLASH_OPT_ATTN_KEY_GROUPS: *value = h->attn_key_groups; return DFLASH_OK;
+    case DFLASH_OPT_INJECT_PASS_ROWS: *value = h->inject_pass_rows; return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }

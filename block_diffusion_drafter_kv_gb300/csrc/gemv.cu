@@ -326,7 +326,7 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
       } else if (s_pos[lr] >= 0) {
         const size_t row_elems = static_cast<size_t>(P.nkv) * P.d;
         const size_t off =
-            ((static_cast<size_t>(layer) * P.max_batch + s_seq[lr]) * P.cap + s_pos[lr]) * row_elems + feat0;
+            (static_cast<size_t>(layer) * P.layer_rows + s_seq[lr]) * row_elems + feat0;
         st16_half((is_v ? P.vc : P.kc) + off, val);
       }
     } break;
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
   float* s_bv = s_inv + C::ROWS;
   int* s_bi = reinterpret_cast<int*>(s_bv + C::ROWS);
   int* s_pos = s_bi + C::ROWS;   // per row of the pass: cache position, or -1 if not written
-  int* s_seq = s_pos + C::ROWS;  // per row of the pass: sequence
+  int* s_seq = s_pos + C::ROWS;  // per row of the pass: its row in a layer of the cache
   uint64_t* full = reinterpret_cast<uint64_t*>(s_seq + C::ROWS);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
@@ -697,8 +697,24 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               pos = -1;
             }
           }
+          // the row of this position in a layer of the cache: sequence-major, or through the
+          // sequence's page table (pages of kPageRows positions)
+          int crow = -1;
+          if (pos >= 0) {
+            if (P.page_table) {
+              const int page = __ldcg(P.page_table + static_cast<size_t>(sq) * P.pages_per_seq + pos / kPageRows);
+              if (page < 0 || page >= P.layer_rows / kPageRows) {
+                raise_flag(P.err, kDevCapacity);
+                pos = -1;
+              } else {
+                crow = page * kPageRows + (pos & (kPageRows - 1));
+              }
+            } else {
+              crow = sq * P.cap + pos;
+            }
+          }
           s_pos[r] = pos;
-          s_seq[r] = sq;
+          s_seq[r] = crow;
         }
       }
       named_bar_sync(1, 128);

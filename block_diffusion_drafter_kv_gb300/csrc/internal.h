@@ -28,6 +28,7 @@ enum GemvOp : int {
 };
 
 constexpr int kMaxAMaps = 16;
+constexpr int kPageRows = 64;      // positions per page of a paged KV cache (= attention key tile)
 constexpr int kMaxCtas = 256;      // workspace partial slots are sized for this many CTAs
 constexpr int kMaxPassRows = 128;  // activation rows per GEMM pass (MMA N = 2 x rows <= 256)
 
@@ -77,6 +78,9 @@ struct GemvParams {
   __half* kc;               // K cache (post-RoPE), fp16: [L][max_batch][cap][nkv][d]
   __half* vc;               // V cache, fp16, same layout
   int nkv, cap, max_batch, layer;
+  int layer_rows;           // rows (positions) per layer of the cache: max_batch * cap, or pages * kPageRows
+  const int* page_table;    // paged cache: [max_batch][pages_per_seq] page ids, or null (sequence-major)
+  int pages_per_seq;
   int* len;
   const int* n_new;
   int rows_per_seq;         // KV: row stride per sequence; draft ops: block size B
@@ -133,6 +137,9 @@ struct AttnParams {
   const int* len;
   int* err;
   int B, nq, nkv, d, cap;
+  const int* page_table;   // paged cache: [max_batch][pages_per_seq] page ids (tile t of a sequence is its
+  int pages_per_seq;       // page t), or null: sequence s's keys start at row s * cap
+  int n_pages;             // pages in the pool (paged cache)
   float scale_log2;        // log2(e) / sqrt(d)
   unsigned long long* tl;  // timeline records (kTlWords per CTA) or null
   int tl_id;

@@ -133,6 +133,20 @@ int dflash_destroy(dflash_handle* h);
 int dflash_bind_state(dflash_handle* h, void* k_cache, void* v_cache, int32_t* len,
                       int32_t* last_token, void* workspace, size_t workspace_bytes);
 
+/* Bind caller-owned state with a paged KV cache, for many ragged sequences sharing one pool:
+ *   k_pool, v_pool    fp16 [L][n_pages * 64][nkv][d]: pages of 64 positions
+ *   page_table        int32 [max_batch][pages_per_seq] on the device: sequence s keeps
+ *                     position p at row page_table[s][p / 64] * 64 + p % 64 of every layer.
+ *                     Read by the kernels at every call: the caller may hand out new pages
+ *                     between calls (the pages a sequence uses must not be shared).
+ *                     pages_per_seq * 64 >= kv_capacity; page ids in [0, n_pages) (others set
+ *                     DFLASH_DEV_CAPACITY and the affected rows are skipped).
+ *   len, last_token, workspace: as for dflash_bind_state.
+ * Every other call behaves as with dflash_bind_state; results are bit-identical. */
+int dflash_bind_state_paged(dflash_handle* h, void* k_pool, void* v_pool, int32_t n_pages,
+                            const int32_t* page_table, int32_t pages_per_seq, int32_t* len,
+                            int32_t* last_token, void* workspace, size_t workspace_bytes);
+
 /* KV injection (theaistack.guide, "L'idea chiave: Il target sa meglio"): for every new
  * position, concatenate the k tapped target hidden states (tap order), fuse them with
  * w_fc, RMSNorm with g_ctx into the context feature c, project c with every layer's
@@ -245,12 +259,21 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
  *   DFLASH_OPT_ATTN_KEY_GROUPS  warps per query head in the attention kernel, 1..2; with 2
  *                             (default; GQA groups of at most 4 heads) the two take
  *                             alternate key tiles and are combined after the key loop
+ *   DFLASH_OPT_INJECT_PASS_ROWS  rows per injection pass: 16, 32, 64 or 128; default 16 x the
+ *                             row groups of max_batch * max_block (at most 128). Every pass
+ *                             streams the fusion and K/V weights once, so wide passes make
+ *                             long prefills cheaper and short injections dearer. Injections
+ *                             at one width give bit-identical K/V however positions are
+ *                             chunked into calls; different widths may differ in the last
+ *                             bits (within the parity tolerance), so set it before the first
+ *                             injection and keep it.
  * Values out of range return DFLASH_E_INVAL and leave the setting unchanged. */
 #define DFLASH_OPT_WAIT_LIMIT_NS 1
 #define DFLASH_OPT_CHAIN_MAX 2
 #define DFLASH_OPT_GEMV_VARIANT 3
 #define DFLASH_OPT_ATTN_SPLIT 4
 #define DFLASH_OPT_ATTN_KEY_GROUPS 5
+#define DFLASH_OPT_INJECT_PASS_ROWS 6
 int dflash_set_option(dflash_handle* h, int32_t option, int64_t value);
 int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value);
 
