@@ -420,13 +420,19 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
   }
 }
 
-// Grid-wide phase barrier: every CTA arrives once per phase after its epilogue work is
-// done; a waiter sees all of that phase's stores. Bounded: false after limit_ns.
 DEV int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Release-add at GPU scope: the CTA's writes ordered before it (by a CTA barrier) become
+// visible to any thread that reads the new count with ld.acquire.gpu.
+DEV void red_release_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Grid-wide phase barrier: every CTA arrives once per phase (a release-add) after its
+// epilogue work is done; a waiter sees all of that phase's stores. Bounded: false after
+// limit_ns.
 DEV bool grid_wait(const int* bar, int target, uint64_t limit_ns) {
   if (ld_acquire_gpu(bar) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -772,9 +778,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               to_rows<C::XLD>(v, m, e, xch, w);
               st16(dst + (ch * 16 + rp.r) * 128 + rp.c0, w);
             }
-            __threadfence();
+            // the CTA barrier orders every thread's partial before thread 0's release
             named_bar_sync(1, 128);
-            if (e == 0) atomicAdd(P.tile_cnt + t, 1);
+            if (e == 0) red_release_gpu(P.tile_cnt + t, 1);
           } else {
             // split tile, finisher: CTA ca, whose last tile this is. The others reach it first
             // (cb) or only (CTAs in between), so ca is usually the last to get here; it keeps
@@ -803,7 +809,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               alive = false;
               break;
             }
-            __threadfence();
+            // the poller's ld.acquire.gpu plus the CTA barrier order the partial loads after
+            // the contributors' releases
             for (int ch = 0; ch < NB; ++ch) {
               float v[16];
               if (NB == 1) {
@@ -907,11 +914,10 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
       }
       // ---------------------------------------------- arrive at this phase's barrier
       fence_proxy_async_global();
-      __threadfence();
       named_bar_sync(1, 128);
       if (e == 0) {
         tl_stamp(tl, 7 + 4 * p);
-        atomicAdd(CH.bar + p, 1);
+        red_release_gpu(CH.bar + p, 1);
       }
     }
   }
