@@ -20,6 +20,7 @@ STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported drafter shape", -3: 
 DEV_TIMEOUT, DEV_CAPACITY, DEV_TOKEN = 1, 2, 4
 OPT_WAIT_LIMIT_NS, OPT_CHAIN_MAX, OPT_GEMV_VARIANT, OPT_ATTN_SPLIT, OPT_ATTN_KEY_GROUPS = 1, 2, 3, 4, 5
 OPT_INJECT_PASS_ROWS = 6
+OPT_ATTN_MODE = 7
 
 
 class DflashConfig(ctypes.Structure):

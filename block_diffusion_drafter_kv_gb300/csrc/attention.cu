@@ -297,6 +297,361 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
   if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
 }
 
+// ---------------------------------------------------------------------------------------
+// Key-split attention over one flat tile list, for ragged or large batches.
+//
+// The key tiles of every (sequence, KV head) pair, pairs in (sequence, head) order, form one
+// list of T tiles cut into G equal contiguous ranges, one per CTA (one CTA per SM): every SM
+// gets the same number of tiles whatever the lengths. A CTA walks its range as segments,
+// one per pair it touches. A pair that lies inside one range is normalised and written by
+// its CTA. A pair cut between CTAs is merged by the last of them to finish (an arrival
+// counter per pair): each writes its unnormalised output and per-row (max, sum) to a slot,
+// 2c for CTA c's first segment and 2c + 1 for its last, and the last to arrive combines the
+// slots in CTA order, so the result does not depend on the order of arrival.
+__host__ __device__ constexpr int attn_flat_fixed_smem(int D, int nw) {
+  // 1024 alignment slack, the ring, full/empty barriers and flags (64 bytes), the second
+  // key group's output and (max, sum) for the combine
+  return 1024 + STAGES * KT * D * 4 + 64 + nw * (D / 8) * 32 * 16 + nw * 32 * 16 + 2 * 128 * 4 + kMaxCtas * 4;
+}
+
+DEV long long flat_begin(int c, long long T, int G) { return static_cast<long long>(c) * T / G; }
+// CTA whose range holds flat tile u.
+DEV int flat_cta_of(long long u, long long T, int G) {
+  return static_cast<int>(((u + 1) * G + T - 1) / T) - 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ AttnParams P) {
+  unsigned long long* tl = P.tl ? P.tl + static_cast<size_t>(blockIdx.x) * kTlWords : nullptr;
+  if (tl && threadIdx.x == 0) {
+    tl[0] = (static_cast<unsigned long long>(TL_ATTN) << 32) | static_cast<unsigned>(P.tl_id);
+    tl[1] = smid();
+    tl_stamp(tl, 2);
+  }
+  constexpr int K_BYTES = KT * D * 2;
+  constexpr int TILE_BYTES = 2 * K_BYTES;
+  constexpr int NT_D = D / 8;
+  const int nw = P.nq / P.nkv;                // warps per key group: the GQA group
+  const int KW = (blockDim.x >> 5) / nw;      // key groups (1 or 2)
+  const int warp = (threadIdx.x >> 5) % nw, kg = (threadIdx.x >> 5) / nw, lane = threadIdx.x & 31;
+  const int r0 = lane >> 2, kq = (lane & 3) * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
+  uint64_t* empty = full + STAGES;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + STAGES * TILE_BYTES + 2 * STAGES * 8);  // [0] abort, [1] last
+  float4* s_o = reinterpret_cast<float4*>(smem + STAGES * TILE_BYTES + 64);
+  float4* s_ml = s_o + nw * NT_D * 32;
+  float* s_rm = reinterpret_cast<float*>(s_ml + nw * 32);  // merge: each row's max
+  float* s_rinv = s_rm + 128;                               // and 1 / normaliser
+  int* s_cs = reinterpret_cast<int*>(s_rinv + 128);         // merge: contributor slots, [G]
+  int* s_pre = s_cs + kMaxCtas;                             // [batch + 1]: tiles per head before sequence s
+
+  const int batch = P.batch, B = P.B, nkv = P.nkv, nq = P.nq;
+  // The kernel before this one (the Q/K/V projection) starts only after the injection of
+  // this step has completed, so len and the injected context keys [0, len) are final here.
+  for (int s = threadIdx.x; s < batch; s += blockDim.x) {
+    int nk = __ldcg(P.len + s) + B;
+    if (nk > P.cap) nk = P.cap;
+    s_pre[s + 1] = (nk + KT - 1) / KT;
+  }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], nw);
+    }
+    s_flag[0] = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&P.kmap);
+    tma_prefetch_desc(&P.vmap);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_pre[0] = 0;
+    for (int s = 0; s < batch; ++s) s_pre[s + 1] += s_pre[s];
+  }
+  __syncthreads();
+
+  const long long T = static_cast<long long>(nkv) * s_pre[batch];
+  const int G = gridDim.x, c = blockIdx.x;
+  const long long T0 = flat_begin(c, T, G);
+  const int n = static_cast<int>(flat_begin(c + 1, T, G) - T0);
+  // flat tile u -> sequence s, head g, tile t of the pair, the pair's tile count nt
+  auto locate = [&](long long u, int& s, int& g, int& t, int& nt) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<long long>(nkv) * s_pre[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    s = lo;
+    nt = s_pre[s + 1] - s_pre[s];
+    const long long r = u - static_cast<long long>(nkv) * s_pre[s];
+    g = static_cast<int>(r / nt);
+    t = static_cast<int>(r - static_cast<long long>(g) * nt);
+  };
+  auto issue = [&](int j, uint64_t pol) {
+    int s, g, t, nt;
+    locate(T0 + j, s, g, t, nt);
+    const int st = j % STAGES;
+    uint8_t* kd = smem + st * TILE_BYTES;
+    uint8_t* vd = kd + K_BYTES;
+    int row = s * P.cap + t * KT;
+    if (P.page_table) {  // tile t of a sequence is its page t
+      const int page = __ldcg(P.page_table + static_cast<size_t>(s) * P.pages_per_seq + t);
+      if (page < 0 || page >= P.n_pages) raise_flag(P.err, kDevCapacity);
+      row = (page < 0 || page >= P.n_pages) ? 0 : page * KT;
+    }
+    mbar_arrive_expect_tx(&full[st], TILE_BYTES);
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_3d(kd + b * KT * 128, &P.kmap, &full[st], b * 64, g, row, pol);
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
+  };
+  const int pre = n < STAGES ? n : STAGES;
+  // tiles entirely below len do not depend on the previous kernel: fetched before waiting
+  auto below_len = [&](int j) {
+    int s, g, t, nt;
+    locate(T0 + j, s, g, t, nt);
+    return (t + 1) * KT <= __ldcg(P.len + s);
+  };
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_last();
+    for (int j = 0; j < pre; ++j)
+      if (below_len(j)) issue(j, pol);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    tl_stamp(tl, 5);
+    const uint64_t pol = policy_evict_last();
+    for (int j = 0; j < pre; ++j)
+      if (!below_len(j)) issue(j, pol);
+  }
+  int issued = pre;  // thread 0: tiles issued so far (in order)
+  // Thread 0 refills the ring in order up to tile `upto`, waiting only for stages whose
+  // previous tile lies before `bound`: tiles the CTA consumes before its next CTA-wide
+  // barrier, so that every wait ends.
+  auto refill = [&](int upto, int bound) {
+    while (issued < n && issued <= upto && issued - STAGES < bound && !s_flag[0]) {
+      const int sj = issued % STAGES;
+      if (issued >= STAGES && !mbar_wait(&empty[sj], ((issued / STAGES) - 1) & 1, P.wait_ns)) {
+        s_flag[0] = 1;
+        raise_flag(P.err, kDevTimeout);
+        break;
+      }
+      issue(issued, policy_evict_last());
+      ++issued;
+    }
+  };
+
+  const size_t slot_floats = static_cast<size_t>(nw) * 16 * (D + 4);
+  bool merged = false;  // thread 0: timeline stamp of the first merge
+  for (int j = 0; j < n;) {
+    int s, g, ta, nt;
+    locate(T0 + j, s, g, ta, nt);
+    const int seg = min(n - j, nt - ta);
+    const bool whole = ta == 0 && seg == nt;
+    int nkeys = __ldcg(P.len + s) + B;
+    if (nkeys > P.cap) nkeys = P.cap;
+    if (threadIdx.x == 0) refill(j + KW + STAGES - 1, j);
+    const int h = g * nw + warp;
+    FaState<D> fa;
+    fa_begin<D>(fa, P.q, static_cast<size_t>(s) * B, static_cast<size_t>(nq) * D, h, B, lane);
+    for (int i = j + ((kg - j % KW) + KW) % KW; i < j + seg; i += KW) {
+      const int st = i % STAGES;
+      if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1, P.wait_ns)) {
+        s_flag[0] = 1;
+        raise_flag(P.err, kDevTimeout);
+      }
+      if (i == 0 && threadIdx.x == 0) tl_stamp(tl, 6);
+      const uint32_t kb = smem_u32(smem + st * TILE_BYTES);
+      fa_tile<D>(fa, kb, kb + K_BYTES, (ta + i - j) * KT, nkeys, P.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      if (threadIdx.x == 0) refill(i + KW + STAGES - 1, j + seg);
+    }
+    fa_end<D>(fa);
+    if (KW > 1) {
+      // the second key group hands its (output, max, sum) to the first, which rescales both
+      // to the larger max and adds them
+      if (kg == 1) {
+#pragma unroll
+        for (int nt2 = 0; nt2 < NT_D; ++nt2)
+          s_o[(warp * NT_D + nt2) * 32 + lane] = make_float4(fa.o[nt2][0], fa.o[nt2][1], fa.o[nt2][2], fa.o[nt2][3]);
+        s_ml[warp * 32 + lane] = make_float4(fa.m[0], fa.m[1], fa.l[0], fa.l[1]);
+      }
+      __syncthreads();
+      if (kg == 0) {
+        const float4 ml = s_ml[warp * 32 + lane];
+        const float mb[2] = {ml.x, ml.y}, lb[2] = {ml.z, ml.w};
+        float ca[2], cb[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float M = fmaxf(fa.m[r], mb[r]);
+          ca[r] = fa.m[r] == -INFINITY ? 0.f : exp2f(fa.m[r] - M);
+          cb[r] = mb[r] == -INFINITY ? 0.f : exp2f(mb[r] - M);
+          fa.l[r] = fa.l[r] * ca[r] + lb[r] * cb[r];
+          fa.m[r] = M;
+        }
+#pragma unroll
+        for (int nt2 = 0; nt2 < NT_D; ++nt2) {
+          const float4 ob = s_o[(warp * NT_D + nt2) * 32 + lane];
+          fa.o[nt2][0] = fa.o[nt2][0] * ca[0] + ob.x * cb[0];
+          fa.o[nt2][1] = fa.o[nt2][1] * ca[0] + ob.y * cb[0];
+          fa.o[nt2][2] = fa.o[nt2][2] * ca[1] + ob.z * cb[1];
+          fa.o[nt2][3] = fa.o[nt2][3] * ca[1] + ob.w * cb[1];
+        }
+      }
+    }
+    if (whole) {
+      // the pair lies in this CTA's range: normalise and write both bf16 planes
+      if (kg == 0) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int slot = r0 + 8 * hr;
+          if (slot >= B) continue;
+          const float inv = fa.l[hr] > 0.f ? 1.f / fa.l[hr] : 0.f;
+          __nv_bfloat16* dst = P.o + (static_cast<size_t>(s) * B + slot) * nq * D + static_cast<size_t>(h) * D;
+#pragma unroll
+          for (int nt2 = 0; nt2 < NT_D; ++nt2) {
+            const float v0 = fa.o[nt2][2 * hr] * inv, v1 = fa.o[nt2][2 * hr + 1] * inv;
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+            *reinterpret_cast<__nv_bfloat162*>(dst + nt2 * 8 + kq) = hi;
+            *reinterpret_cast<__nv_bfloat162*>(dst + static_cast<size_t>(P.o_lo) * nq * D + nt2 * 8 + kq) = lo;
+          }
+        }
+      }
+    } else {
+      // a cut pair: this CTA's part to its slot, then count it in
+      const long long base = static_cast<long long>(nkv) * s_pre[s] + static_cast<long long>(g) * nt;
+      float* slot_p = P.part + (2 * static_cast<size_t>(c) + (j == 0 ? 0 : 1)) * slot_floats;
+      if (kg == 0) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int rr = warp * 16 + r0 + 8 * hr;
+          if (r0 + 8 * hr >= B) continue;
+#pragma unroll
+          for (int nt2 = 0; nt2 < NT_D; ++nt2)
+            __stcg(reinterpret_cast<float2*>(slot_p + static_cast<size_t>(rr) * D + nt2 * 8 + kq),
+                   make_float2(fa.o[nt2][2 * hr], fa.o[nt2][2 * hr + 1]));
+          if ((lane & 3) == 0)
+            __stcg(reinterpret_cast<float4*>(slot_p + static_cast<size_t>(nw) * 16 * D + rr * 4),
+                   make_float4(fa.m[hr], fa.l[hr], 0.f, 0.f));
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int c_first = flat_cta_of(base, T, G), c_last = flat_cta_of(base + nt - 1, T, G);
+        int n_c = 0;  // CTAs with a part of the pair (CTAs with an empty range have none)
+        for (int cc = c_first; cc <= c_last; ++cc) n_c += flat_begin(cc + 1, T, G) > flat_begin(cc, T, G);
+        __threadfence();
+        const int old = atomicAdd(P.cnt + s * nkv + g, 1);
+        const int last = old == n_c - 1;
+        if (last) {
+          P.cnt[s * nkv + g] = 0;
+          __threadfence();
+        }
+        s_flag[1] = last;
+      }
+      __syncthreads();
+      if (s_flag[1]) {
+        if (threadIdx.x == 0 && !merged) tl_stamp(tl, 8);
+        merged = true;
+        // Combine the parts in CTA order: out = sum_c exp2(m_c - M) o_c / sum_c exp2(m_c - M) l_c.
+        // The contributors' slots first, then each row's max and normaliser, then the rows in
+        // 16-float blocks with every contributor's loads of a block in flight together.
+        const int c_first = flat_cta_of(base, T, G), c_last = flat_cta_of(base + nt - 1, T, G);
+        const int nk = c_last - c_first + 1;
+        const int R = nw * 16;
+        for (int k = threadIdx.x; k < nk; k += blockDim.x) {
+          const int cc = c_first + k;
+          const long long b0 = flat_begin(cc, T, G);
+          s_cs[k] = flat_begin(cc + 1, T, G) > b0 ? 2 * cc + (b0 >= base ? 0 : 1) : -1;
+        }
+        __syncthreads();
+        for (int rr = threadIdx.x; rr < R; rr += blockDim.x) {
+          if ((rr & 15) >= B) continue;
+          float M = -INFINITY, den = 0.f;
+#pragma unroll 4
+          for (int k = 0; k < nk; ++k) {
+            const int sl = s_cs[k];
+            if (sl < 0) continue;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(P.part + sl * slot_floats + static_cast<size_t>(R) * D + rr * 4));
+            if (ml.x == -INFINITY) continue;
+            if (ml.x > M) {
+              den = den * exp2f(M - ml.x) + ml.y;
+              M = ml.x;
+            } else {
+              den += ml.y * exp2f(ml.x - M);
+            }
+          }
+          s_rm[rr] = M;
+          s_rinv[rr] = den > 0.f ? 1.f / den : 0.f;
+        }
+        __syncthreads();
+        for (int it = threadIdx.x; it < R * (D / 16); it += blockDim.x) {
+          const int rr = it / (D / 16), d = (it % (D / 16)) * 16;
+          const int w = rr >> 4, slot = rr & 15;
+          if (slot >= B) continue;
+          const float M = s_rm[rr], inv = s_rinv[rr];
+          float acc[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+#pragma unroll 2
+          for (int k = 0; k < nk; ++k) {
+            const int sl = s_cs[k];
+            if (sl < 0) continue;
+            const float* sp = P.part + sl * slot_floats;
+            const float mc = __ldcg(sp + static_cast<size_t>(R) * D + rr * 4);
+            float4 pv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pv[q] = __ldcg(reinterpret_cast<const float4*>(sp + static_cast<size_t>(rr) * D + d + 4 * q));
+            const float wc = mc == -INFINITY ? 0.f : exp2f(mc - M) * inv;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q] += wc * pv[q].x;
+              acc[4 * q + 1] += wc * pv[q].y;
+              acc[4 * q + 2] += wc * pv[q].z;
+              acc[4 * q + 3] += wc * pv[q].w;
+            }
+          }
+          __nv_bfloat16* dst =
+              P.o + (static_cast<size_t>(s) * B + slot) * nq * D + static_cast<size_t>(g * nw + w) * D + d;
+          uint4 hv[2], lv[2];
+          __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(hv);
+          __nv_bfloat162* lp = reinterpret_cast<__nv_bfloat162*>(lv);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            hp[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            const float2 f = __bfloat1622float2(hp[q]);
+            lp[q] = __floats2bfloat162_rn(acc[2 * q] - f.x, acc[2 * q + 1] - f.y);
+          }
+          reinterpret_cast<uint4*>(dst)[0] = hv[0];
+          reinterpret_cast<uint4*>(dst)[1] = hv[1];
+          reinterpret_cast<uint4*>(dst + static_cast<size_t>(P.o_lo) * nq * D)[0] = lv[0];
+          reinterpret_cast<uint4*>(dst + static_cast<size_t>(P.o_lo) * nq * D)[1] = lv[1];
+        }
+        if (threadIdx.x == 0) tl_stamp(tl, 9);
+      }
+    }
+    __syncthreads();  // the combine buffers and s_flag[1] are reused by the next segment
+    j += seg;
+  }
+  if (threadIdx.x == 0) {
+    tl_stamp(tl, 7);
+    // after an abandoned wait, the copies still in flight land before the CTA exits
+    if (s_flag[0])
+      for (int q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
+        if (!mbar_wait(&full[q % STAGES], (q / STAGES) & 1, P.wait_ns)) break;
+    tl_stamp(tl, kTlExit);
+  }
+}
+
 // Dynamic shared memory: the tile ring (which holds this CTA's staged partials after the
 // key loop), its barriers, and the merge inputs from every CTA of the cluster.
 static int attn_smem(int D, int nw, int split) {
@@ -305,8 +660,16 @@ static int attn_smem(int D, int nw, int split) {
 }
 static int attn_smem_max(int D) { return attn_smem(D, 8, 16); }
 
+int attn_flat_smem(int D, int nw, int batch) { return attn_flat_fixed_smem(D, nw) + (batch + 1) * 4; }
+
 int attn_set_attributes() {
   cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_flat_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_flat_smem(128, 4, kAttnFlatMaxBatch));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_flat_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_flat_smem(64, 8, kAttnFlatMaxBatch));
 #define DFL_ATTN_ATTR(D)                                                                                   \
   if (e == cudaSuccess)                                                                                    \
     e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_max(D)); \
@@ -356,6 +719,29 @@ static int launch_d(const AttnParams& p, int batch, int split, cudaStream_t stre
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   return static_cast<int>(cudaLaunchKernelEx(&cfg, attn_kernel<D>, p));
+}
+
+template <int D>
+static int launch_flat_d(const AttnParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
+  const int group = p.nq / p.nkv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas, 1, 1);
+  cfg.blockDim = dim3(32 * group * p.key_groups);
+  cfg.dynamicSmemBytes = attn_flat_smem(D, group, p.batch);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, attn_flat_kernel<D>, p));
+}
+
+int launch_attention_flat(const AttnParams& p, int n_ctas, cudaStream_t stream, bool pdl) {
+  if (p.batch < 1 || p.batch > kAttnFlatMaxBatch || n_ctas < 1 || n_ctas > kMaxCtas) return static_cast<int>(cudaErrorInvalidValue);
+  if (p.d == 128) return launch_flat_d<128>(p, n_ctas, stream, pdl);
+  if (p.d == 64) return launch_flat_d<64>(p, n_ctas, stream, pdl);
+  return static_cast<int>(cudaErrorInvalidValue);
 }
 
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl) {

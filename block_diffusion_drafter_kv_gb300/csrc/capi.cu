@@ -30,6 +30,7 @@ struct WsLayout {
   size_t err, tile_cnt, cta_cnt, seq_cnt, rope_cos, rope_sin, part, best_v, best_i;
   size_t ss_fc, ss_x, ss_emb, cfeat, x, xg, q, o, act, vpart_v, vpart_i, chain_bar;
   size_t tgt_xg, tgt_ss, tgt_g;  // fused target-side verification
+  size_t attn_part, attn_cnt;    // flat key-split attention: partial slots, per-pair counters
   size_t total;
   int R;          // draft rows allocated (multiple of 16)
   int max_tiles;  // tile counters
@@ -82,6 +83,8 @@ WsLayout layout_of(const dflash_config& c) {
   L.tgt_xg = take(2 * R * static_cast<size_t>(c.target_hidden) * 2);
   L.tgt_ss = take(R * 4);
   L.tgt_g = take(R * 4);
+  L.attn_part = take(static_cast<size_t>(2) * kMaxCtas * (nq / c.n_kv_heads) * 16 * (d + 4) * 4);
+  L.attn_cnt = take(static_cast<size_t>(c.max_batch) * c.n_kv_heads * 4);
   L.total = off;
   return L;
 }
@@ -164,6 +167,7 @@ struct dflash_handle {
   unsigned long long wait_ns = kDefaultWaitLimitNs;  // limit of every wait inside a kernel
   int attn_wide = 0;           // clusters of 12 the device holds at once (0: none)
   int attn_key_groups = 2;     // warps per query head in the attention kernel (taking alternate tiles)
+  int attn_mode = 0;           // 0: clusters of 12 where they fit, else the flat key split; 1: clusters; 2: flat
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -710,11 +714,26 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     const int pairs = batch * c.n_kv_heads;
     int split = h->n_sms / pairs;
     split = (split >= 12 && h->attn_wide >= pairs) ? 12 : std::max(1, std::min(8, split));
+    A.wait_ns = h->wait_ns;
+    A.key_groups = (c.n_heads / c.n_kv_heads <= 4) ? h->attn_key_groups : 1;
+    // Where there are not two SMs per pair (many sequences), one flat list of every pair's
+    // key tiles split evenly over the SMs balances ragged lengths; otherwise clusters.
+    const bool flat = batch <= kAttnFlatMaxBatch &&
+                      (h->attn_mode == 2 || (h->attn_mode == 0 && h->attn_split == 0 && h->n_sms < 2 * pairs));
+    if (flat) {
+      const int G = std::min(h->n_sms, kMaxCtas);
+      A.batch = batch;
+      A.part = h->at<float>(h->L.attn_part);
+      A.cnt = h->at<int>(h->L.attn_cnt);
+      A.tl = tl_take(h, G);
+      A.tl_id = h->tl_launch++;
+      if (launch_attention_flat(A, G, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+      note_launch(h, st);
+      return DFLASH_OK;
+    }
     if (h->attn_split > 0) split = h->attn_split;
     A.tl = tl_take(h, static_cast<long long>(split) * c.n_kv_heads * batch);
     A.tl_id = h->tl_launch++;
-    A.wait_ns = h->wait_ns;
-    A.key_groups = (c.n_heads / c.n_kv_heads <= 4) ? h->attn_key_groups : 1;
     if (launch_attention(A, batch, split, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
     note_launch(h, st);
     return DFLASH_OK;
@@ -937,7 +956,8 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
                                {L.tile_cnt, static_cast<size_t>(L.max_tiles) * 4},
                                {L.cta_cnt, 4},
                                {L.seq_cnt, static_cast<size_t>(h->cfg.max_batch) * 4},
-                               {L.chain_bar, static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4}};
+                               {L.chain_bar, static_cast<size_t>(kChainSlots) * (kMaxPhases + 4) * 4},
+                               {L.attn_cnt, static_cast<size_t>(h->cfg.max_batch) * h->cfg.n_kv_heads * 4}};
     for (const auto& sp : spans)
       if (cudaMemsetAsync(h->ws + sp[0], 0, sp[1], st) != cudaSuccess) return DFLASH_E_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return DFLASH_E_CUDA;
@@ -972,6 +992,10 @@ int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
       if (value != 16 && value != 32 && value != 64 && value != 128) return DFLASH_E_INVAL;
       h->inject_pass_rows = static_cast<int>(value);
       return DFLASH_OK;
+    case DFLASH_OPT_ATTN_MODE:
+      if (value < 0 || value > 2) return DFLASH_E_INVAL;
+      h->attn_mode = static_cast<int>(value);
+      return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }
@@ -985,6 +1009,7 @@ int dflash_get_option(const dflash_handle* h, int32_t option, int64_t* value) {
     case DFLASH_OPT_ATTN_SPLIT: *value = h->attn_split; return DFLASH_OK;
     case DFLASH_OPT_ATTN_KEY_GROUPS: *value = h->attn_key_groups; return DFLASH_OK;
     case DFLASH_OPT_INJECT_PASS_ROWS: *value = h->inject_pass_rows; return DFLASH_OK;
+    case DFLASH_OPT_ATTN_MODE: *value = h->attn_mode; return DFLASH_OK;
   }
   return DFLASH_E_INVAL;
 }

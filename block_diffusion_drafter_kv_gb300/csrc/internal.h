@@ -145,8 +145,14 @@ struct AttnParams {
   int tl_id;
   unsigned long long wait_ns;  // limit of every wait in the kernel
   int key_groups;          // 1, or 2 (GQA groups of at most 4 heads): warps taking alternate tiles
+  // flat key split (attn_flat_kernel) only
+  int batch;
+  float* part;             // [2 * CTAs] slots of (group*16 rows x (d outputs), then (max, sum, 0, 0) per row)
+  int* cnt;                // [batch][nkv] arrival counters, zero between launches
 };
+constexpr int kAttnFlatMaxBatch = 4096;  // sequences per flat-split launch (a shared-memory prefix table)
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
+int launch_attention_flat(const AttnParams& p, int n_ctas, cudaStream_t stream, bool pdl);
 int attn_set_attributes();
 int attn_resident_clusters(int split);
 

@@ -80,6 +80,22 @@ def test_full_size_block_sweep_draft_matches_oracle(full, prefilled, B):
     check_draft(full.oracle.draft(prefilled.st, B), g_dr, g_lo, g_tr)
 
 
+def test_full_size_flat_attention_matches_oracle(full, prefilled):
+    """The flat key-split attention kernel (the default for many or long sequences) on the
+    single-sequence context: 33 key tiles per KV head cut over every SM, so each head is
+    merged from several CTAs' parts. Every layer's residual, the logits and the drafts
+    against the oracle."""
+    from gpu_util import check_draft
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    d, B = full.drafter, W_QWEN3_8B.block
+    d.set_option(BND.OPT_ATTN_MODE, 2)
+    try:
+        g_dr, g_lo, g_tr = _draft(full, B)
+    finally:
+        d.set_option(BND.OPT_ATTN_MODE, 0)
+    check_draft(full.oracle.draft(prefilled.st, B), g_dr, g_lo, g_tr)
+
+
 def test_full_size_step_matches_oracle(full, prefilled):
     from gpu_util import check_draft
     w, s, d = W_QWEN3_8B, full.s, full.drafter

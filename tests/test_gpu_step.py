@@ -138,6 +138,20 @@ def test_step_loop_with_one_key_group(tiny, B):
         d.set_option(BND.OPT_ATTN_KEY_GROUPS, 2)
 
 
+@pytest.mark.parametrize("B", [16, 4])
+def test_step_loop_with_flat_attention(tiny, B):
+    """The same loop with the flat key-split attention kernel (every pair's key tiles in one
+    list over one CTA per SM). The tiny cache has fewer tiles than there are CTAs, so every
+    pair of more than one tile is cut between CTAs and merged by the last to arrive."""
+    from block_diffusion_drafter_kv_gb300 import binding as BND
+    d = tiny.drafter
+    d.set_option(BND.OPT_ATTN_MODE, 2)
+    try:
+        _step_loop(tiny, B)
+    finally:
+        d.set_option(BND.OPT_ATTN_MODE, 0)
+
+
 def _step_loop(tiny, B):
     from gpu_util import check_draft, max_rel, LAYER_RTOL
     s, w = tiny.s, W_TINY
@@ -232,8 +246,9 @@ def test_options_round_trip(tiny):
     d = tiny.drafter
     assert d.get_option(BND.OPT_WAIT_LIMIT_NS) == 2_000_000_000
     assert d.get_option(BND.OPT_CHAIN_MAX) == 8
+    assert d.get_option(BND.OPT_ATTN_MODE) == 0
     for opt, bad in ((BND.OPT_WAIT_LIMIT_NS, 10), (BND.OPT_CHAIN_MAX, 9), (BND.OPT_GEMV_VARIANT, 6),
-                     (BND.OPT_ATTN_SPLIT, 17), (99, 1)):
+                     (BND.OPT_ATTN_SPLIT, 17), (BND.OPT_ATTN_MODE, 3), (BND.OPT_ATTN_MODE, -1), (99, 1)):
         with pytest.raises(BND.DFlashError):
             d.set_option(opt, bad)
     d.set_option(BND.OPT_CHAIN_MAX, 3)
