@@ -308,10 +308,12 @@ __global__ void __launch_bounds__(256) attn_kernel(const __grid_constant__ AttnP
 // counter per pair): each writes its unnormalised output and per-row (max, sum) to a slot,
 // 2c for CTA c's first segment and 2c + 1 for its last, and the last to arrive combines the
 // slots in CTA order, so the result does not depend on the order of arrival.
+constexpr int FST = 3;                                    // ring depth of the flat kernel
+constexpr int kFlatHdr = (2 * FST * 8 + 16 + 15) / 16 * 16;  // its full/empty barriers and flags
 __host__ __device__ constexpr int attn_flat_fixed_smem(int D, int nw) {
-  // 1024 alignment slack, the ring, full/empty barriers and flags (64 bytes), the second
-  // key group's output and (max, sum) for the combine
-  return 1024 + STAGES * KT * D * 4 + 64 + nw * (D / 8) * 32 * 16 + nw * 32 * 16 + 2 * 128 * 4 + kMaxCtas * 4;
+  // 1024 alignment slack, the ring, barriers and flags, the second key group's output and
+  // (max, sum) for the combine, the merge's row statistics and contributor slots
+  return 1024 + FST * KT * D * 4 + kFlatHdr + nw * (D / 8) * 32 * 16 + nw * 32 * 16 + 2 * 128 * 4 + kMaxCtas * 4;
 }
 
 DEV long long flat_begin(int c, long long T, int G) { return static_cast<long long>(c) * T / G; }
@@ -337,10 +339,10 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
   const int r0 = lane >> 2, kq = (lane & 3) * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
-  uint64_t* empty = full + STAGES;
-  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + STAGES * TILE_BYTES + 2 * STAGES * 8);  // [0] abort, [1] last
-  float4* s_o = reinterpret_cast<float4*>(smem + STAGES * TILE_BYTES + 64);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + FST * TILE_BYTES);
+  uint64_t* empty = full + FST;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + FST * TILE_BYTES + 2 * FST * 8);  // [0] abort, [1] last
+  float4* s_o = reinterpret_cast<float4*>(smem + FST * TILE_BYTES + kFlatHdr);
   float4* s_ml = s_o + nw * NT_D * 32;
   float* s_rm = reinterpret_cast<float*>(s_ml + nw * 32);  // merge: each row's max
   float* s_rinv = s_rm + 128;                               // and 1 / normaliser
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
     s_pre[s + 1] = (nk + KT - 1) / KT;
   }
   if (threadIdx.x == 0) {
-    for (int st = 0; st < STAGES; ++st) {
+    for (int st = 0; st < FST; ++st) {
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], nw);
     }
@@ -392,10 +394,8 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
     g = static_cast<int>(r / nt);
     t = static_cast<int>(r - static_cast<long long>(g) * nt);
   };
-  auto issue = [&](int j, uint64_t pol) {
-    int s, g, t, nt;
-    locate(T0 + j, s, g, t, nt);
-    const int st = j % STAGES;
+  auto issue_at = [&](int j, int s, int g, int t, uint64_t pol) {
+    const int st = j % FST;
     uint8_t* kd = smem + st * TILE_BYTES;
     uint8_t* vd = kd + K_BYTES;
     int row = s * P.cap + t * KT;
@@ -410,15 +410,23 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
 #pragma unroll
     for (int b = 0; b < D / 64; ++b) tma_load_3d(vd + b * KT * 128, &P.vmap, &full[st], b * 64, g, row, pol);
   };
-  const int pre = n < STAGES ? n : STAGES;
+  // K/V read once per call: streamed through L2 unless the layer's cache is small enough to
+  // stay there until the next step (16 MB, one eighth of L2, per layer)
+  const uint64_t kv_pol = T * TILE_BYTES > (16ll << 20) ? policy_evict_first() : policy_evict_last();
+  const int pre = n < FST ? n : FST;
   // tiles entirely below len do not depend on the previous kernel: fetched before waiting
   auto below_len = [&](int j) {
     int s, g, t, nt;
     locate(T0 + j, s, g, t, nt);
     return (t + 1) * KT <= __ldcg(P.len + s);
   };
+  auto issue = [&](int j, uint64_t pol) {
+    int s, g, t, nt;
+    locate(T0 + j, s, g, t, nt);
+    issue_at(j, s, g, t, pol);
+  };
   if (threadIdx.x == 0) {
-    const uint64_t pol = policy_evict_last();
+    const uint64_t pol = kv_pol;
     for (int j = 0; j < pre; ++j)
       if (below_len(j)) issue(j, pol);
   }
@@ -426,24 +434,35 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     tl_stamp(tl, 5);
-    const uint64_t pol = policy_evict_last();
+    const uint64_t pol = kv_pol;
     for (int j = 0; j < pre; ++j)
       if (!below_len(j)) issue(j, pol);
   }
   int issued = pre;  // thread 0: tiles issued so far (in order)
+  // thread 0: (sequence, head, tile, tiles of the pair) of tile `issued`, advanced in order
+  int cs = 0, cg = 0, ct = 0, cnt = 1;
+  if (threadIdx.x == 0 && issued < n) locate(T0 + issued, cs, cg, ct, cnt);
   // Thread 0 refills the ring in order up to tile `upto`, waiting only for stages whose
   // previous tile lies before `bound`: tiles the CTA consumes before its next CTA-wide
   // barrier, so that every wait ends.
   auto refill = [&](int upto, int bound) {
-    while (issued < n && issued <= upto && issued - STAGES < bound && !s_flag[0]) {
-      const int sj = issued % STAGES;
-      if (issued >= STAGES && !mbar_wait(&empty[sj], ((issued / STAGES) - 1) & 1, P.wait_ns)) {
+    while (issued < n && issued <= upto && issued - FST < bound && !s_flag[0]) {
+      const int sj = issued % FST;
+      if (issued >= FST && !mbar_wait(&empty[sj], ((issued / FST) - 1) & 1, P.wait_ns)) {
         s_flag[0] = 1;
         raise_flag(P.err, kDevTimeout);
         break;
       }
-      issue(issued, policy_evict_last());
+      issue_at(issued, cs, cg, ct, kv_pol);
       ++issued;
+      if (++ct == cnt) {
+        ct = 0;
+        if (++cg == nkv) {
+          cg = 0;
+          ++cs;
+          if (cs < batch) cnt = s_pre[cs + 1] - s_pre[cs];
+        }
+      }
     }
   };
 
@@ -456,13 +475,13 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
     const bool whole = ta == 0 && seg == nt;
     int nkeys = __ldcg(P.len + s) + B;
     if (nkeys > P.cap) nkeys = P.cap;
-    if (threadIdx.x == 0) refill(j + KW + STAGES - 1, j);
+    if (threadIdx.x == 0) refill(j + KW + FST - 1, j);
     const int h = g * nw + warp;
     FaState<D> fa;
     fa_begin<D>(fa, P.q, static_cast<size_t>(s) * B, static_cast<size_t>(nq) * D, h, B, lane);
     for (int i = j + ((kg - j % KW) + KW) % KW; i < j + seg; i += KW) {
-      const int st = i % STAGES;
-      if (!s_flag[0] && !mbar_wait(&full[st], (i / STAGES) & 1, P.wait_ns)) {
+      const int st = i % FST;
+      if (!s_flag[0] && !mbar_wait(&full[st], (i / FST) & 1, P.wait_ns)) {
         s_flag[0] = 1;
         raise_flag(P.err, kDevTimeout);
       }
@@ -471,7 +490,7 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
       fa_tile<D>(fa, kb, kb + K_BYTES, (ta + i - j) * KT, nkeys, P.scale_log2, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (threadIdx.x == 0) refill(i + KW + STAGES - 1, j + seg);
+      if (threadIdx.x == 0) refill(i + KW + FST - 1, j + seg);
     }
     fa_end<D>(fa);
     if (KW > 1) {
@@ -646,8 +665,8 @@ __global__ void __launch_bounds__(256) attn_flat_kernel(const __grid_constant__ 
     tl_stamp(tl, 7);
     // after an abandoned wait, the copies still in flight land before the CTA exits
     if (s_flag[0])
-      for (int q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q)
-        if (!mbar_wait(&full[q % STAGES], (q / STAGES) & 1, P.wait_ns)) break;
+      for (int q = issued > FST ? issued - FST : 0; q < issued; ++q)
+        if (!mbar_wait(&full[q % FST], (q / FST) & 1, P.wait_ns)) break;
     tl_stamp(tl, kTlExit);
   }
 }

@@ -716,10 +716,11 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     split = (split >= 12 && h->attn_wide >= pairs) ? 12 : std::max(1, std::min(8, split));
     A.wait_ns = h->wait_ns;
     A.key_groups = (c.n_heads / c.n_kv_heads <= 4) ? h->attn_key_groups : 1;
-    // Where there are not two SMs per pair (many sequences), one flat list of every pair's
-    // key tiles split evenly over the SMs balances ragged lengths; otherwise clusters.
+    // Clusters of 12 where every pair gets one at once (few sequences: the merge runs in
+    // distributed shared memory); otherwise one flat list of every pair's key tiles split
+    // evenly over the SMs, which balances ragged and long contexts.
     const bool flat = batch <= kAttnFlatMaxBatch &&
-                      (h->attn_mode == 2 || (h->attn_mode == 0 && h->attn_split == 0 && h->n_sms < 2 * pairs));
+                      (h->attn_mode == 2 || (h->attn_mode == 0 && h->attn_split == 0 && split < 12));
     if (flat) {
       const int G = std::min(h->n_sms, kMaxCtas);
       A.batch = batch;

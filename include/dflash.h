@@ -267,11 +267,11 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
  *                             chunked into calls; different widths may differ in the last
  *                             bits (within the parity tolerance), so set it before the first
  *                             injection and keep it.
- *   DFLASH_OPT_ATTN_MODE      attention kernel: 0 (default) a cluster of CTAs per (sequence,
- *                             KV head) splitting its keys where the SMs give each pair at least
- *                             two, otherwise one flat list of every pair's key tiles split evenly
- *                             over the SMs (many, ragged sequences); 1 always clusters; 2 always
- *                             the flat split (batches of at most 4096 sequences)
+ *   DFLASH_OPT_ATTN_MODE      attention kernel: 0 (default) a cluster of 12 CTAs per (sequence,
+ *                             KV head) splitting its keys where every pair gets one at once,
+ *                             otherwise one flat list of every pair's key tiles split evenly
+ *                             over the SMs (several, ragged or long contexts); 1 always
+ *                             clusters; 2 always the flat split (at most 4096 sequences)
  * Values out of range return DFLASH_E_INVAL and leave the setting unchanged. */
 #define DFLASH_OPT_WAIT_LIMIT_NS 1
 #define DFLASH_OPT_CHAIN_MAX 2
