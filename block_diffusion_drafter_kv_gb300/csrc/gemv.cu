@@ -233,35 +233,36 @@ DEV void rope_row(float (&val)[16], const float (&cs)[16], const float (&sn)[16]
   }
 }
 
-// Per-tile epilogue inputs that do not depend on the accumulator, loaded before waiting for
-// it so that the epilogue after the MMAs has no dependent global loads (single row group).
+// Epilogue inputs of one 16-row chunk that do not depend on the accumulator, loaded before
+// the accumulator (and, on a split tile, the other CTAs' partials) so that their global
+// round trips overlap: FC / RESID: a = gains of the lane's 16 features, b = the residual the
+// tile updates (RESID); KV / QKV: a, b = RoPE cos / sin at the lane's row position.
 struct EpiPre {
   bool have;
-  float g[16];             // FC / RESID: gains of the lane's 16 features
-  float x[16];             // RESID: the residual the tile updates (lane's row and features)
-  float cs[16], sn[16];    // KV / QKV: RoPE cos / sin at the lane's row position
+  float a[16], b[16];
 };
 
 template <int NB, int MINB>
-DEV void epilogue_prefetch(const GemvParams& P, int t, int e, const int* s_pos, EpiPre& pre) {
-  pre.have = NB == 1 && MINB == 1;  // a halved register budget cannot hold them across the wait
+DEV void epilogue_prefetch(const GemvParams& P, int t, int ch, int e, const int* s_pos, EpiPre& pre) {
+  pre.have = MINB == 1;  // a halved register budget cannot hold them across the wait
   if (!pre.have) return;
   const RowPos rp = row_pos(e);
+  const int lr = ch * 16 + rp.r;
   if (P.op == OP_RESID || P.op == OP_FC) {
-    ld16_bf16(P.gain + t * 128 + rp.c0, pre.g);
+    ld16_bf16(P.gain + t * 128 + rp.c0, pre.a);
     if (P.op == OP_RESID) {
-      const int gr = P.grow0 + rp.r;
+      const int gr = P.grow0 + lr;
       if (gr < P.n_valid) {
-        ld16(P.y + static_cast<size_t>(gr) * P.y_ld + t * 128 + rp.c0, pre.x);
+        ld16(P.y + static_cast<size_t>(gr) * P.y_ld + t * 128 + rp.c0, pre.b);
       } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pre.x[k] = 0.f;
+        for (int k = 0; k < 16; ++k) pre.b[k] = 0.f;
       }
     }
   } else if (P.op == OP_KV || P.op == OP_QKV) {
     const int mi = map_of_tile(P, t);
     if (P.op == OP_KV ? !(mi & 1) : mi < 2)
-      rope_tables_row(max(s_pos[rp.r], 0), rp.c0, P.d, P.rope_cos, P.rope_sin, pre.cs, pre.sn);
+      rope_tables_row(max(s_pos[lr], 0), rp.c0, P.d, P.rope_cos, P.rope_sin, pre.a, pre.b);
   }
 }
 
@@ -289,7 +290,7 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
       float g[16], w[16];
       if (pre.have) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) g[k] = pre.g[k];
+        for (int k = 0; k < 16; ++k) g[k] = pre.a[k];
       } else {
         ld16_bf16(P.gain + t * 128 + c0, g);
       }
@@ -314,7 +315,7 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
       for (int k = 0; k < 16; ++k) val[k] = v[k] * inv;
       if (!is_v) {
         if (pre.have) {
-          rope_row(val, pre.cs, pre.sn, c0, P.d);
+          rope_row(val, pre.a, pre.b, c0, P.d);
         } else {
           float cs[16], sn[16];
           rope_tables_row(max(s_pos[lr], 0), c0, P.d, P.rope_cos, P.rope_sin, cs, sn);
@@ -336,8 +337,8 @@ DEV void epilogue_rows(const GemvParams& P, int t, int chunk, float (&v)[16], in
       if (pre.have) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          xo[k] = pre.x[k];
-          g[k] = pre.g[k];
+          xo[k] = pre.b[k];
+          g[k] = pre.a[k];
         }
       } else {
         ld16_bf16(P.gain + t * 128 + c0, g);
@@ -739,7 +740,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
           const int acc = lt & 1;
           EpiPre pre;
-          epilogue_prefetch<NB, C::MINB>(P, t, e, s_pos, pre);
+          epilogue_prefetch<NB, C::MINB>(P, t, 0, e, s_pos, pre);
           if (e == 0) s_misc[1 + acc] = mbar_wait(&tfull[acc], (lt >> 1) & 1, WL) ? 1 : 0;
           named_bar_sync(1, 128);
           if (!s_misc[1 + acc]) {
@@ -754,6 +755,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           if (ca == cb) {
             for (int ch = 0; ch < NB; ++ch) {
               float v[16], w[16];
+              if (ch > 0) epilogue_prefetch<NB, C::MINB>(P, t, ch, e, s_pos, pre);
               tmem_ld_acc(taddr, ch, split, v);
               if (ch == NB - 1) {
                 tc_fence_before();
@@ -762,9 +764,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               to_rows<C::XLD>(v, m, e, xch, w);
               epilogue_rows<NB>(P, t, ch, w, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
-          } else if (c != ca) {
-            // split tile, contributor: its partial goes to its slot ([ROWS][128] fp32, row
-            // layout), then it is counted in
+          } else if (c != ca || NB > 1) {
+            // split tile, contributor (with several row groups, every CTA of the tile): its
+            // partial goes to its slot ([ROWS][128] fp32, row layout), then it is counted in
             const int slot = part_slot(c, t, U, Gp, P.KB);
             float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
             const RowPos rp = row_pos(e);
@@ -781,10 +783,58 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             // the CTA barrier orders every thread's partial before thread 0's release
             named_bar_sync(1, 128);
             if (e == 0) red_release_gpu(P.tile_cnt + t, 1);
+            if (NB > 1) {
+              // Several row groups: the finishing is shared. Every CTA of the tile whose last
+              // tile this is (ca and the CTAs wholly inside it, all done with their units at
+              // about the same time) waits for every partial, then finishes row chunks
+              // ch = k, k + n_sh, ... (k = c - ca), adding the partials in CTA order.
+              const uint32_t tile_end = static_cast<uint32_t>(t + 1) * P.KB;
+              if (unit_begin(c + 1, U, Gp) <= tile_end) {
+                const int n_c = cb - ca + 1;
+                const int n_sh = (unit_begin(cb + 1, U, Gp) <= tile_end ? cb : cb - 1) - ca + 1;
+                if (e == 0) {
+                  const bool ok = grid_wait(P.tile_cnt + t, n_c, WL);
+                  // each sharer counts itself past the partials; the last clears the counter
+                  if (ok && atomicAdd(P.tile_cnt + t, 1) == n_c + n_sh - 1) P.tile_cnt[t] = 0;
+                  s_misc[0] = ok ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                if (!s_misc[0]) {
+                  if (e == 0) raise_flag(err, kDevTimeout);
+                  alive = false;
+                  break;
+                }
+                constexpr int PR = C::MINB == 1 ? 6 : 4;
+                for (int ch = c - ca; ch < NB; ch += n_sh) {
+                  EpiPre pc;
+                  epilogue_prefetch<NB, C::MINB>(P, t, ch, e, s_pos, pc);
+                  auto part_row = [&](int cc) {
+                    return P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                           (ch * 16 + rp.r) * 128 + rp.c0;
+                  };
+                  float v[16];
+                  ld16(part_row(ca), v);
+                  for (int cc0 = ca + 1; cc0 <= cb; cc0 += PR) {
+                    float a[PR][16];
+#pragma unroll
+                    for (int q2 = 0; q2 < PR; ++q2)
+                      if (cc0 + q2 <= cb) ld16(part_row(cc0 + q2), a[q2]);
+#pragma unroll
+                    for (int q2 = 0; q2 < PR; ++q2)
+                      if (cc0 + q2 <= cb) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) v[k] += a[q2][k];
+                      }
+                  }
+                  epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pc);
+                }
+              }
+            }
           } else {
-            // split tile, finisher: CTA ca, whose last tile this is. The others reach it first
-            // (cb) or only (CTAs in between), so ca is usually the last to get here; it keeps
-            // its own sum, waits for the cb - ca other partials and adds them in CTA order.
+            // split tile of a single-row-group pass, finisher: CTA ca, whose last tile this is.
+            // The others reach it first (cb) or only (CTAs in between), so ca is usually the
+            // last to get here; it keeps its own sum, waits for the cb - ca other partials and
+            // adds them in CTA order.
             const RowPos rp = row_pos(e);
             float own[16];
             if (NB == 1) {  // own accumulator out of TMEM while the others finish
@@ -812,6 +862,18 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             // the poller's ld.acquire.gpu plus the CTA barrier order the partial loads after
             // the contributors' releases
             for (int ch = 0; ch < NB; ++ch) {
+              if (ch > 0) epilogue_prefetch<NB, C::MINB>(P, t, ch, e, s_pos, pre);
+              // the others' partials, up to PR CTAs' loads in flight per round; the first
+              // round is issued before this CTA's own sum is read out
+              constexpr int PR = C::MINB == 1 ? 8 : 4;
+              auto part_row = [&](int cc) {
+                return P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                       (ch * 16 + rp.r) * 128 + rp.c0;
+              };
+              float a[PR][16];
+#pragma unroll
+              for (int q2 = 0; q2 < PR; ++q2)
+                if (ca + 1 + q2 <= cb) ld16(part_row(ca + 1 + q2), a[q2]);
               float v[16];
               if (NB == 1) {
 #pragma unroll
@@ -825,16 +887,12 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                 }
                 to_rows<C::XLD>(a0, m, e, xch, v);
               }
-              // the others' partials, up to PR CTAs' loads in flight per round
-              constexpr int PR = C::MINB == 1 ? 8 : 4;
               for (int cc0 = ca + 1; cc0 <= cb; cc0 += PR) {
-                float a[PR][16];
+                if (cc0 > ca + 1) {
 #pragma unroll
-                for (int q2 = 0; q2 < PR; ++q2)
-                  if (cc0 + q2 <= cb)
-                    ld16(P.part + static_cast<size_t>(part_slot(cc0 + q2, t, U, Gp, P.KB)) * C::ROWS * 128 +
-                             (ch * 16 + rp.r) * 128 + rp.c0,
-                         a[q2]);
+                  for (int q2 = 0; q2 < PR; ++q2)
+                    if (cc0 + q2 <= cb) ld16(part_row(cc0 + q2), a[q2]);
+                }
 #pragma unroll
                 for (int q2 = 0; q2 < PR; ++q2)
                   if (cc0 + q2 <= cb) {
