@@ -138,7 +138,7 @@ bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uin
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int nb_index(int nb) { return nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : 3; }
+int nb_index(int nb) { return nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : nb == 8 ? 3 : 4; }
 int nb_for_rows(int rows) {
   int nb = 1;
   while (nb * 16 < rows && nb * 16 < kMaxPassRows) nb *= 2;
@@ -182,8 +182,8 @@ struct dflash_handle {
   int* last_token = nullptr;
   uint8_t* ws = nullptr;
   WsLayout L{};
-  CUtensorMap m_xg[4]{}, m_cfeat[4]{}, m_act[4]{}, m_o[4]{};  // by nb_index, over both planes
-  CUtensorMap m_txg[4]{};  // the target's normed-hidden operand (fused verification), by nb_index
+  CUtensorMap m_xg[5]{}, m_cfeat[5]{}, m_act[5]{}, m_o[5]{};  // by nb_index, over both planes
+  CUtensorMap m_txg[5]{};  // the target's normed-hidden operand (fused verification), by nb_index
   std::vector<CUtensorMap> m_kcache, m_vcache;
   int last_launches = 0;
   std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
@@ -389,7 +389,7 @@ int bind_common(dflash_handle* h, void* k_cache, void* v_cache, int layer_rows, 
     return DFLASH_E_CUDA;
   const uint64_t H = c.hidden, d = c.head_dim;
   bool ok = true;
-  for (int k = 0; k < 4 && ok; ++k) {
+  for (int k = 0; k < 5 && ok; ++k) {
     const uint32_t box = 16u << k;
     ok = enc2d(&h->m_xg[k], h->ws + L.xg, H, 2 * L.R, box) &&
          enc2d(&h->m_cfeat[k], h->ws + L.cfeat, H, 2 * kMaxPassRows, box) &&
@@ -990,7 +990,7 @@ int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
       h->attn_key_groups = static_cast<int>(value);
       return DFLASH_OK;
     case DFLASH_OPT_INJECT_PASS_ROWS:
-      if (value != 16 && value != 32 && value != 64 && value != 128) return DFLASH_E_INVAL;
+      if (value != 16 && value != 32 && value != 64 && value != 128 && value != 256) return DFLASH_E_INVAL;
       h->inject_pass_rows = static_cast<int>(value);
       return DFLASH_OK;
     case DFLASH_OPT_ATTN_MODE:

@@ -31,15 +31,17 @@ namespace dfl {
 //
 // Activations are carried as two bf16 planes, x = hi + lo with hi = bf16(x) and
 // lo = bf16(x - hi), so that a bf16 tensor-core product sees x to about 16 significant
-// bits: the B tile of a k-box holds the ROWS high rows followed by the ROWS low rows, one
-// MMA of N = 2*ROWS multiplies both, and the epilogue adds the two halves of the fp32
-// accumulator. The weight bytes streamed are unchanged; the MMA work doubles, which costs
-// nothing while the kernel waits on HBM. Operands that are exact in bf16 (the target's
-// hidden states) are loaded as the high plane only, with an MMA of N = ROWS.
+// bits: the B tile of a k-box holds the ROWS high rows followed by the ROWS low rows. Up to
+// 128 rows one MMA of N = 2*ROWS multiplies both and the epilogue adds the two halves of
+// the fp32 accumulator; at 256 rows (N would exceed 256) one MMA per plane accumulates into
+// the same columns. The weight bytes streamed are unchanged; the MMA work doubles, which
+// costs nothing while the kernel waits on HBM. Operands that are exact in bf16 (the
+// target's hidden states) are loaded as the high plane only, with an MMA of N = ROWS.
 template <int NB, int KSUB, int STAGES_, int MINB_>
 struct GemvCfg {
   static constexpr int ROWS = 16 * NB;                // activation rows of a pass
-  static constexpr int NCOL = 2 * ROWS;               // MMA N with both planes
+  static constexpr bool PLANES_IN_N = 2 * ROWS <= 256;  // both planes in one MMA's N
+  static constexpr int NCOL = PLANES_IN_N ? 2 * ROWS : ROWS;  // accumulator columns
   static constexpr int KS = KSUB;
   static constexpr int STAGES = STAGES_;
   static constexpr int MINB = MINB_;
@@ -54,7 +56,7 @@ struct GemvCfg {
   static constexpr int EPI_BYTES = 16 * XLD * 4 + 5 * ROWS * 4;  // xch, inv, best v/i, row pos/seq
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 32;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC2 = idesc_bf16_f32(128, NCOL);  // high and low planes
+  static constexpr uint32_t IDESC2 = idesc_bf16_f32(128, NCOL);  // both planes (PLANES_IN_N)
   static constexpr uint32_t IDESC1 = idesc_bf16_f32(128, ROWS);  // high plane only
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(TMEM_COLS <= 512, "TMEM columns");
@@ -624,7 +626,8 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem + acc * C::NCOL;
-          const uint32_t idesc = P.b_lo ? C::IDESC2 : C::IDESC1;
+          const uint32_t idesc = (P.b_lo && C::PLANES_IN_N) ? C::IDESC2 : C::IDESC1;
+          const bool lo_mma = P.b_lo && !C::PLANES_IN_N;  // the low plane as a second MMA
           for (uint32_t u = ub; u < ue; ++u, ++i) {
             const uint32_t s = i % C::STAGES, r = i / C::STAGES;
             if (!mbar_wait(&full[s], r & 1, WL)) {
@@ -638,10 +641,12 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
 #pragma unroll
             for (int j = 0; j < C::KS; ++j)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc_mma_bf16(d_tmem, smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32),
-                            smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), idesc,
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc_k_sw128(a0 + j * C::A_SUB + kk * 32);
+                tc_mma_bf16(d_tmem, ad, smem_desc_k_sw128(b0 + j * C::B_SUB + kk * 32), idesc,
                             (u > ub || j > 0 || kk > 0) ? 1u : 0u);
+                if (lo_mma) tc_mma_bf16(d_tmem, ad, smem_desc_k_sw128(b0 + j * C::B_SUB + C::B_PLANE + kk * 32), idesc, 1u);
+              }
             tc_commit(&empty[s]);
           }
           if (ok) tc_commit(&tfull[acc]);
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         }
       }
       named_bar_sync(1, 128);
-      const bool split = P.b_lo != 0;
+      const bool split = P.b_lo != 0 && C::PLANES_IN_N;  // planes in separate accumulator columns
       // Accumulator of 16 rows (chunk ch): high-plane columns, plus the low-plane columns.
       auto tmem_ld_acc = [&](uint32_t taddr, int ch, bool two, float (&v)[16]) {
         tmem_ld16(taddr + ch * 16, v);
@@ -1029,17 +1034,18 @@ static int set_attr() {
   X(8, 8, 1, 3, 1)              \
   X(9, 2, 4, 2, 1)              \
   X(10, 4, 2, 3, 1)             \
-  X(11, 8, 2, 2, 1)
+  X(11, 8, 2, 2, 1)             \
+  X(12, 16, 1, 2, 1)
 
 // Several k-boxes per stage for every row count (contiguous bytes per weight row, and about
 // 128 KB of weights in flight per SM where shared memory allows); the 1-box variants 0 and
 // 6..8 serve phases whose k-block count the box count does not divide.
 int gemv_variant(int nb, int pref) {
   if (nb == 1) return (pref >= 0 && pref <= 5) ? pref : 3;
-  return nb == 2 ? 9 : nb == 4 ? 10 : 11;
+  return nb == 2 ? 9 : nb == 4 ? 10 : nb == 8 ? 11 : 12;
 }
 
-int gemv_variant_ksub1(int nb) { return nb == 1 ? 0 : nb == 2 ? 6 : nb == 4 ? 7 : 8; }
+int gemv_variant_ksub1(int nb) { return nb == 1 ? 0 : nb == 2 ? 6 : nb == 4 ? 7 : nb == 8 ? 8 : 12; }
 
 int gemv_variant_ksub(int v) {
 #define DFL_KS(ID, NB, KS, ST, MB) if (v == ID) return KS;

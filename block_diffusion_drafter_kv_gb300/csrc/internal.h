@@ -30,7 +30,7 @@ enum GemvOp : int {
 constexpr int kMaxAMaps = 16;
 constexpr int kPageRows = 64;      // positions per page of a paged KV cache (= attention key tile)
 constexpr int kMaxCtas = 256;      // workspace partial slots are sized for this many CTAs
-constexpr int kMaxPassRows = 128;  // activation rows per GEMM pass (MMA N = 2 x rows <= 256)
+constexpr int kMaxPassRows = 256;  // activation rows per GEMM pass (MMA N <= 256 per plane)
 
 struct GemvParams {
   CUtensorMap amap[kMaxAMaps];  // weight maps, box 64 (k) x 64 (rows), 128-byte swizzle

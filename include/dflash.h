@@ -235,7 +235,7 @@ int dflash_verify_greedy_hidden(dflash_handle* h, const void* target_hidden, con
 
 /* Weight-streaming bf16 GEMM of the draft path, exposed for testing the engine alone:
  * Y[r][m] = sum_k X[r][k] * W[m][k] in fp32 accumulation.
- *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (any rows; passes of 128),
+ *   W  bf16 [n_out][K] (K multiple of 64), X bf16 [rows][K] (any rows; passes of 256),
  *   Y  fp32 [rows][n_out] out. Uses the handle's bound workspace for split-K partials. */
 int dflash_linear_bf16(dflash_handle* h, const void* W, int32_t n_out, int32_t K, const void* X,
                        int32_t rows, float* Y, void* stream);
@@ -259,8 +259,8 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
  *   DFLASH_OPT_ATTN_KEY_GROUPS  warps per query head in the attention kernel, 1..2; with 2
  *                             (default; GQA groups of at most 4 heads) the two take
  *                             alternate key tiles and are combined after the key loop
- *   DFLASH_OPT_INJECT_PASS_ROWS  rows per injection pass: 16, 32, 64 or 128; default 16 x the
- *                             row groups of max_batch * max_block (at most 128). Every pass
+ *   DFLASH_OPT_INJECT_PASS_ROWS  rows per injection pass: 16, 32, 64, 128 or 256; default 16 x
+ *                             the row groups of max_batch * max_block (at most 256). Every pass
  *                             streams the fusion and K/V weights once, so wide passes make
  *                             long prefills cheaper and short injections dearer. Injections
  *                             at one width give bit-identical K/V however positions are
