@@ -104,14 +104,14 @@ def _passes(rows, width):
 def launch_plan(s, batch, B, tau, n_ctx, n_sms=152, one_pass=False, chain_max=8):
     """Launch order of one step by call: (label, kind, bytes, flops). kind "gemv" marks the
     chained kernel (one launch runs up to `chain_max` phases, the handle's
-    DFLASH_OPT_CHAIN_MAX, for one pass of at most 128 rows); attention is a launch of its own
+    DFLASH_OPT_CHAIN_MAX, for one pass of at most 256 rows); attention is a launch of its own
     between chains. Injection runs in passes of a width fixed by max_batch * max_block.
     Mirrors the library's grouping. With one_pass every projection covers all rows at once:
     the method's own traffic, each weight once."""
     ab = attn_bytes_flops(s, batch, B, n_ctx)
     rows = batch * B
     nb = 1
-    while nb * 16 < min(rows, 128):
+    while nb * 16 < min(rows, 256):
         nb *= 2
     inject = []
     for _, pr in _passes(rows, rows if one_pass else 16 * nb):   # tau accepted rows per sequence, padded to B
@@ -125,7 +125,7 @@ def launch_plan(s, batch, B, tau, n_ctx, n_sms=152, one_pass=False, chain_max=8)
         if seg == "attn":
             draft.append(("attn", "attn", *ab))
             continue
-        for _, pr in _passes(rows, rows if one_pass else 128):
+        for _, pr in _passes(rows, rows if one_pass else 256):
             pj = proj_bytes_flops(s, 1, pr, 1)
             if "lm_head" in seg:   # the LM head of a pass covers its rows' drafted slots
                 pj["lm_head"] = proj_bytes_flops(s, pr // B if pr >= B else 1, B, 1)["lm_head"]
@@ -703,6 +703,49 @@ def run_cuda(a):
             reset()
         stream.synchronize()
 
+    # ---------------------------------------------------------------- in-graph attention (timeline)
+    # The traced pass serialises launches; here one graph-replayed step records per-CTA
+    # %globaltimer stamps instead, and each attention launch is charged the time from the
+    # last CTA exit of the launch before it to its own last CTA exit (the time it adds to
+    # the step, programmatic overlap included).
+    attn_graph = None
+    if a.trace_steps > 0:
+        rec = torch.zeros(32768, 37, dtype=torch.int64, device="cuda")
+        dr.timeline(rec)
+        g_tl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_tl, stream=stream):
+            inject_draft()
+            plant_verify()
+        used = dr.timeline_used()
+        dr.timeline(None)
+        if used <= rec.shape[0]:
+            with torch.cuda.stream(stream):
+                reset()
+                g_tl.replay()   # warm
+                reset()
+                rec.zero_()
+                g_tl.replay()
+                reset()
+            stream.synchronize()
+            r = rec[:used].cpu().numpy()
+            lid = r[:, 0] & 0xFFFFFFFF
+            kind = r[:, 0] >> 32
+            ends = {int(l): int(r[lid == l, 36].max()) for l in np.unique(lid)}
+            order = sorted(ends)
+            adds = [ends[l] - ends[order[i - 1]] for i, l in enumerate(order)
+                    if i > 0 and int(kind[lid == l][0]) == 2]
+            if adds:
+                ab_bytes = attn_bytes_flops(s, batch, B, n_avg)[0]
+                us = 1e-3 * float(np.mean(adds))
+                attn_graph = {"us_per_layer": round(us, 2), "bytes": ab_bytes,
+                              "achieved_gbs": round(ab_bytes / (us * 1e-6) / 1e9, 1),
+                              "frac_of_hbm": round(ab_bytes / (us * 1e-6) / 1e9 / hbm, 4),
+                              "layers": len(adds),
+                              "how": "one graph-replayed step with per-CTA timeline stamps: last CTA exit "
+                                     "of each attention launch minus that of the launch before it"}
+                log(f"[bench] attention in graph: {us:.1f} us per layer")
+        del g_tl, rec
+
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if not a.no_e2e:
@@ -792,7 +835,8 @@ def run_cuda(a):
             "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block, "fused_target_verify": fused,
             "prefill": prefill,
             "draft_flatness": (max(draft_by_block.values()) / min(draft_by_block.values())) if draft_by_block else None,
-            "roofline": roof, "step_roofline": step_roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "step_roofline": step_roof, "kernels": kern, "attention_in_graph": attn_graph,
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": per_step_launches * a.steps, "launches_per_step": launches,
             "clocks": clk, "device_error": err,
         }

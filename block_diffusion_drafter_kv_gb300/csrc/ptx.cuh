@@ -88,6 +88,12 @@ DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+// Prefetch `bytes` (a multiple of 16) from global address p (16-byte aligned) into L2: a
+// hint with nothing to wait for.
+DEV void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
 DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
                      uint64_t policy) {
   asm volatile(

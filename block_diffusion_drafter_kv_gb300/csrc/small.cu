@@ -116,14 +116,18 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyParams P) {
     tl[1] = smid();
     tl_stamp(tl, 2);
   }
-  pdl_wait();
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) tl_stamp(tl, 5);
   const int chunk = blockIdx.x, i = blockIdx.y, s = blockIdx.z;
   const int B = P.B, V = P.V;
   const float* row = P.logits + (static_cast<size_t>(s) * B + i) * V;
   const int c0 = chunk * P.chunk_len;
   const int c1 = min(V, c0 + P.chunk_len);
+  // The chunk into L2 while the kernel before this one finishes. Only a hint: the logits are
+  // read after the wait below, and L2 holds whatever that kernel writes meanwhile. (Rows
+  // start 16-byte aligned when V is a multiple of 4; chunks are multiples of 1024 logits.)
+  if (threadIdx.x == 0 && (V & 3) == 0 && c1 > c0) bulk_prefetch_l2(row + c0, static_cast<uint32_t>(c1 - c0) * 4u);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) tl_stamp(tl, 5);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   if ((V & 3) == 0) {

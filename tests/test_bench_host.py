@@ -12,7 +12,7 @@ from synth import WORKLOADS, weight_bytes
 
 @pytest.mark.parametrize("name,n_inject,n_draft", [
     ("qwen3-8b-b1-ctx2048-B16", 1, 12),          # one 16-row pass; embed, qkv, 5 x (attn, chain)
-    ("qwen3-8b-b32-ctx512..8192-B16", 4, 30),    # 512 rows in 128-row passes
+    ("qwen3-8b-b32-ctx512..8192-B16", 2, 18),    # 512 rows in 256-row passes
     ("llama3.1-8b-L8-b4-ctx32768-B16", 1, 18),   # 64 rows: one pass; 8 layers
 ])
 def test_launch_plan_shape(name, n_inject, n_draft):
