@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libdflash.so")
-SOURCES = ["gemv.cu", "attention.cu", "small.cu", "capi.cu", "verify_noalloc.cu"]
+SOURCES = ["gemv.cu", "attention.cu", "attn_tc.cu", "small.cu", "capi.cu", "verify_noalloc.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

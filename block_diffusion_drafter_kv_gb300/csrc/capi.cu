@@ -83,7 +83,8 @@ WsLayout layout_of(const dflash_config& c) {
   L.tgt_xg = take(2 * R * static_cast<size_t>(c.target_hidden) * 2);
   L.tgt_ss = take(R * 4);
   L.tgt_g = take(R * 4);
-  L.attn_part = take(static_cast<size_t>(2) * kMaxCtas * (nq / c.n_kv_heads) * 16 * (d + 4) * 4);
+  // flat attention slots: a head's 16 slots x its query heads, or two KV heads' (tensor-core kernel)
+  L.attn_part = take(static_cast<size_t>(2) * kMaxCtas * 2 * (nq / c.n_kv_heads) * 16 * (d + 4) * 4);
   L.attn_cnt = take(static_cast<size_t>(c.max_batch) * c.n_kv_heads * 4);
   L.total = off;
   return L;
@@ -128,10 +129,10 @@ bool enc3d_hidden(CUtensorMap* m, const void* base, uint64_t Ht, uint64_t rows, 
 
 // One layer's fp16 K or V cache [rows = max_batch*cap][nkv][d], box 64 (d, 128 bytes) x 1 head
 // x 64 keys.
-bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows) {
+bool enc3d_cache(CUtensorMap* m, const void* base, uint64_t d, uint64_t nkv, uint64_t rows, uint32_t box_rows = 64) {
   cuuint64_t dims[3] = {d, nkv, rows};
   cuuint64_t strides[2] = {d * 2, nkv * d * 2};
-  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -167,7 +168,8 @@ struct dflash_handle {
   unsigned long long wait_ns = kDefaultWaitLimitNs;  // limit of every wait inside a kernel
   int attn_wide = 0;           // clusters of 12 the device holds at once (0: none)
   int attn_key_groups = 2;     // warps per query head in the attention kernel (taking alternate tiles)
-  int attn_mode = 0;           // 0: clusters of 12 where they fit, else the flat key split; 1: clusters; 2: flat
+  int attn_mode = 0;           // 0: clusters of 12 where they fit, else the flat key split; 1: clusters;
+                               // 2: flat (tensor cores where the shape allows); 3: flat on mma.sync
   // weight descriptors
   CUtensorMap m_fc{}, m_lm{};
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -185,6 +187,7 @@ struct dflash_handle {
   CUtensorMap m_xg[5]{}, m_cfeat[5]{}, m_act[5]{}, m_o[5]{};  // by nb_index, over both planes
   CUtensorMap m_txg[5]{};  // the target's normed-hidden operand (fused verification), by nb_index
   std::vector<CUtensorMap> m_kcache, m_vcache;
+  std::vector<CUtensorMap> m_kcache32, m_vcache32;  // the same caches in boxes of 32 positions
   int last_launches = 0;
   std::vector<cudaEvent_t> trace_ev;  // caller-owned events recorded around launches, or empty
   unsigned long long* tl_buf = nullptr;  // caller-owned timeline buffer, or null
@@ -319,7 +322,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->inject_pass_rows = 16 * nb_for_rows(std::min(cfg->max_batch * cfg->max_block, kMaxPassRows));
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-      gemv_set_attributes() != 0 || attn_set_attributes() != 0) {
+      gemv_set_attributes() != 0 || attn_set_attributes() != 0 || attn_tc_set_attributes() != 0) {
     delete h;
     return DFLASH_E_CUDA;
   }
@@ -399,10 +402,14 @@ int bind_common(dflash_handle* h, void* k_cache, void* v_cache, int layer_rows, 
   }
   h->m_kcache.resize(c.n_layers);
   h->m_vcache.resize(c.n_layers);
+  h->m_kcache32.resize(c.n_layers);
+  h->m_vcache32.resize(c.n_layers);
   const size_t layer_elems = static_cast<size_t>(layer_rows) * c.n_kv_heads * d;
   for (int l = 0; l < c.n_layers && ok; ++l) {
     ok = enc3d_cache(&h->m_kcache[l], h->kc + l * layer_elems, d, c.n_kv_heads, layer_rows) &&
-         enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, layer_rows);
+         enc3d_cache(&h->m_vcache[l], h->vc + l * layer_elems, d, c.n_kv_heads, layer_rows) &&
+         enc3d_cache(&h->m_kcache32[l], h->kc + l * layer_elems, d, c.n_kv_heads, layer_rows, 32) &&
+         enc3d_cache(&h->m_vcache32[l], h->vc + l * layer_elems, d, c.n_kv_heads, layer_rows, 32);
   }
   if (!ok) return DFLASH_E_CUDA;
   h->bound = true;
@@ -694,6 +701,8 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     AttnParams A{};
     A.kmap = h->m_kcache[l];
     A.vmap = h->m_vcache[l];
+    A.kmap32 = h->m_kcache32[l];
+    A.vmap32 = h->m_vcache32[l];
     A.q = h->at<__half>(h->L.q);
     A.o = h->at<__nv_bfloat16>(h->L.o);
     A.o_lo = R;
@@ -720,7 +729,7 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
     // distributed shared memory); otherwise one flat list of every pair's key tiles split
     // evenly over the SMs, which balances ragged and long contexts.
     const bool flat = batch <= kAttnFlatMaxBatch &&
-                      (h->attn_mode == 2 || (h->attn_mode == 0 && h->attn_split == 0 && split < 12));
+                      (h->attn_mode >= 2 || (h->attn_mode == 0 && h->attn_split == 0 && split < 12));
     if (flat) {
       const int G = std::min(h->n_sms, kMaxCtas);
       A.batch = batch;
@@ -728,7 +737,13 @@ int dflash_draft_block(dflash_handle* h, int32_t batch, int32_t block, int32_t* 
       A.cnt = h->at<int>(h->L.attn_cnt);
       A.tl = tl_take(h, G);
       A.tl_id = h->tl_launch++;
-      if (launch_attention_flat(A, G, st, h->trace_ev.empty()) != 0) return DFLASH_E_CUDA;
+      // the tensor-core kernel where every head pair gets two SMs or more (long contexts:
+      // few segment switches, whose pipeline drain it pays); the mma.sync one for many sequences
+      const bool tc = attn_tc_supported(A) &&
+                      (h->attn_mode == 2 || (h->attn_mode == 0 && batch * c.n_kv_heads <= h->n_sms));
+      if ((tc ? launch_attention_flat_tc(A, G, st, h->trace_ev.empty())
+              : launch_attention_flat(A, G, st, h->trace_ev.empty())) != 0)
+        return DFLASH_E_CUDA;
       note_launch(h, st);
       return DFLASH_OK;
     }
@@ -994,7 +1009,7 @@ int dflash_set_option(dflash_handle* h, int32_t option, int64_t value) {
       h->inject_pass_rows = static_cast<int>(value);
       return DFLASH_OK;
     case DFLASH_OPT_ATTN_MODE:
-      if (value < 0 || value > 2) return DFLASH_E_INVAL;
+      if (value < 0 || value > 3) return DFLASH_E_INVAL;
       h->attn_mode = static_cast<int>(value);
       return DFLASH_OK;
   }

@@ -131,6 +131,7 @@ int gemv_set_attributes();
 struct AttnParams {
   CUtensorMap kmap;  // 3-D over this layer's fp16 K cache: {d, nkv, max_batch*cap}, box {64, 1, 64}
   CUtensorMap vmap;  // 3-D over this layer's fp16 V cache: box {64, 1, 64}
+  CUtensorMap kmap32, vmap32;  // the same in boxes of 32 positions (tensor-core flat kernel)
   const __half* q;   // [rows][nq*d], row = s*B + i, post-RoPE, fp16
   __nv_bfloat16* o;  // [rows][nq*d] high plane; the low plane follows o_lo rows further on
   int o_lo;
@@ -153,6 +154,11 @@ struct AttnParams {
 constexpr int kAttnFlatMaxBatch = 4096;  // sequences per flat-split launch (a shared-memory prefix table)
 int launch_attention(const AttnParams& p, int batch, int split, cudaStream_t stream, bool pdl);
 int launch_attention_flat(const AttnParams& p, int n_ctas, cudaStream_t stream, bool pdl);
+// The flat split on the tcgen05 tensor cores (head dim 128, 4 query heads per KV head,
+// B <= 16); attn_tc_supported says whether p qualifies.
+bool attn_tc_supported(const AttnParams& p);
+int launch_attention_flat_tc(const AttnParams& p, int n_ctas, cudaStream_t stream, bool pdl);
+int attn_tc_set_attributes();
 int attn_set_attributes();
 int attn_resident_clusters(int split);
 

@@ -270,8 +270,13 @@ int dflash_read_device_error(dflash_handle* h, int32_t* flags, int32_t clear, vo
  *   DFLASH_OPT_ATTN_MODE      attention kernel: 0 (default) a cluster of 12 CTAs per (sequence,
  *                             KV head) splitting its keys where every pair gets one at once,
  *                             otherwise one flat list of every pair's key tiles split evenly
- *                             over the SMs (several, ragged or long contexts); 1 always
- *                             clusters; 2 always the flat split (at most 4096 sequences)
+ *                             over the SMs (several, ragged or long contexts): on the tcgen05
+ *                             tensor cores (head dim 128, 4 query heads per KV head, an even
+ *                             KV head count, at most 1024 sequences) where batch x KV heads is
+ *                             at most the SM count, else on the mma.sync path; 1 always
+ *                             clusters; 2 always the flat split, on the tensor cores where the
+ *                             shape allows (at most 4096 sequences); 3 the flat split on the
+ *                             mma.sync path
  * Values out of range return DFLASH_E_INVAL and leave the setting unchanged. */
 #define DFLASH_OPT_WAIT_LIMIT_NS 1
 #define DFLASH_OPT_CHAIN_MAX 2

@@ -80,15 +80,17 @@ def test_full_size_block_sweep_draft_matches_oracle(full, prefilled, B):
     check_draft(full.oracle.draft(prefilled.st, B), g_dr, g_lo, g_tr)
 
 
-def test_full_size_flat_attention_matches_oracle(full, prefilled):
-    """The flat key-split attention kernel (the default for many or long sequences) on the
+@pytest.mark.parametrize("mode,B", [(2, 16), (2, 4), (3, 16)])
+def test_full_size_flat_attention_matches_oracle(full, prefilled, mode, B):
+    """The flat key-split attention kernels (the default for many or long sequences) on the
     single-sequence context: 33 key tiles per KV head cut over every SM, so each head is
-    merged from several CTAs' parts. Every layer's residual, the logits and the drafts
-    against the oracle."""
+    merged from several CTAs' parts. Mode 2 takes the tcgen05 kernel (head dim 128, groups
+    of 4 query heads; at B = 4 most of its 64 query rows are unused slots), mode 3 the
+    mma.sync one. Every layer's residual, the logits and the drafts against the oracle."""
     from gpu_util import check_draft
     from block_diffusion_drafter_kv_gb300 import binding as BND
-    d, B = full.drafter, W_QWEN3_8B.block
-    d.set_option(BND.OPT_ATTN_MODE, 2)
+    d = full.drafter
+    d.set_option(BND.OPT_ATTN_MODE, mode)
     try:
         g_dr, g_lo, g_tr = _draft(full, B)
     finally:
@@ -141,15 +143,17 @@ def test_full_size_step_matches_oracle(full, prefilled):
 # checks sampled sequences of a full-size GPU run. Sequences the oracle does not check get
 # N(0,1) hidden states drawn on the device.
 
-def _run_sampled(w, seed, sampled, oracle_dtype=np.float64, chunk=4096):
+def _run_sampled(w, seed, sampled, oracle_dtype=np.float64, chunk=4096, attn_mode=0):
     from gpu_util import Setup, check_draft, max_rel, LAYER_RTOL
     from oracle.dflash_ref import Oracle
+    from block_diffusion_drafter_kv_gb300 import binding as BND
     s, B, batch = w.shape, w.block, w.batch
     ctx = I.ragged_ctx(w, seed)
     sampled = list(sampled(ctx))
     cap = int(ctx.max()) + 64
     S = Setup(w, seed=seed, max_batch=batch, kv_capacity=cap)
     d = S.drafter
+    d.set_option(BND.OPT_ATTN_MODE, attn_mode)
     rps = int(ctx.max())
     hid = torch.empty(s.n_taps, batch * rps, s.target_hidden, dtype=torch.bfloat16, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(seed)
@@ -205,13 +209,15 @@ def _run_sampled(w, seed, sampled, oracle_dtype=np.float64, chunk=4096):
         assert int(d.last_token[q]) == r.last_token
 
 
-def test_batched_ragged_sampled_sequences_match_oracle():
+@pytest.mark.parametrize("attn_mode", [0, 2])
+def test_batched_ragged_sampled_sequences_match_oracle(attn_mode):
     """Batch 32, context lengths uniform in [512, 8192], B = 16, per-sequence agreement
     rates. Sampled by index: one sequence in each group of eight (the rows of one 128-row
     projection pass, and of one 256-row pass in pairs of groups), plus the sequence with
-    the longest context (the most key tiles per attention CTA)."""
+    the longest context (the most key tiles per attention CTA). Attention by the default
+    choice for this batch (the mma.sync flat split) and by the tcgen05 flat kernel."""
     from synth import W_BATCHED
-    _run_sampled(W_BATCHED, 31, lambda ctx: sorted({3, 12, 21, 30, int(np.argmax(ctx))}))
+    _run_sampled(W_BATCHED, 31, lambda ctx: sorted({3, 12, 21, 30, int(np.argmax(ctx))}), attn_mode=attn_mode)
 
 
 def test_long_context_llama_shaped_sequence_matches_oracle():

@@ -9,25 +9,36 @@ import torch
 
 from synth import W_TINY
 from synth import inputs as I
+from synth.configs import DrafterShape
 
 pytestmark = pytest.mark.gpu
 SEED = 55
 BATCH, CAP, PPS = 3, 256, 4      # pages_per_seq * 64 = kv_capacity
+# head dim 128, 4 query heads per KV head, 2 KV heads: the shape of the tensor-core flat
+# attention kernel, at a size the tests run in seconds
+TINY128 = DrafterShape(hidden=512, n_heads=8, n_kv_heads=2, head_dim=128, n_layers=2,
+                       intermediate=1536, vocab=1024, n_taps=3, target_hidden=512, rope_theta=1e6)
 
 
-@pytest.fixture(scope="module")
-def pair():
+@pytest.fixture(scope="module", params=[(W_TINY.shape, 0), (TINY128, 2), (TINY128, 3)],
+                ids=["tiny-auto", "d128-flat-tensor-core", "d128-flat-mma-sync"])
+def pair(request):
+    """Two drafters of one shape and attention mode (DFLASH_OPT_ATTN_MODE): a sequence-major
+    cache and a paged one. Mode 2 takes the tcgen05 flat kernel, which reads the cache in
+    32-position steps (two per page); mode 3 the mma.sync flat kernel."""
     from block_diffusion_drafter_kv_gb300 import binding as B
     from block_diffusion_drafter_kv_gb300.build import build
     build()
-    s = W_TINY.shape
+    s, mode = request.param
     w = I.make_weights(s, SEED).to("cuda")
     flat = B.Drafter(s, w, max_block=16, max_batch=BATCH, kv_capacity=CAP)
     n_pages = BATCH * PPS + 5
     perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(SEED))[: BATCH * PPS]
     pt = perm.view(BATCH, PPS).to(torch.int32).cuda()
     paged = B.Drafter(s, w, max_block=16, max_batch=BATCH, kv_capacity=CAP, n_pages=n_pages, page_table=pt)
-    return flat, paged, pt
+    for d in (flat, paged):
+        d.set_option(B.OPT_ATTN_MODE, mode)
+    return flat, paged, pt, s
 
 
 def _gather(paged, pt, seq, upto):
@@ -35,10 +46,10 @@ def _gather(paged, pt, seq, upto):
     return paged.k_cache[:, rows], paged.v_cache[:, rows]
 
 
-def _step(d, batch, B, noise, drafted_in=None):
+def _step(d, s, batch, B, noise, drafted_in=None):
     drafted = torch.full((batch, B - 1), -1, dtype=torch.int32, device="cuda")
-    logits = torch.full((batch, B - 1, W_TINY.shape.vocab), float("nan"), device="cuda")
-    trace = torch.full((W_TINY.shape.n_layers + 1, batch * B, W_TINY.shape.hidden), float("nan"), device="cuda")
+    logits = torch.full((batch, B - 1, s.vocab), float("nan"), device="cuda")
+    trace = torch.full((s.n_layers + 1, batch * B, s.hidden), float("nan"), device="cuda")
     d.draft(batch, B, drafted, logits, trace)
     acc = torch.zeros(batch, dtype=torch.int32, device="cuda")
     com = torch.zeros(batch, B, dtype=torch.int32, device="cuda")
@@ -48,8 +59,7 @@ def _step(d, batch, B, noise, drafted_in=None):
 
 
 def test_paged_cache_is_bit_identical_to_sequence_major(pair):
-    flat, paged, pt = pair
-    s = W_TINY.shape
+    flat, paged, pt, s = pair
     ctx = [70, 130, 37]          # ragged: 2, 3 and 1 pages
     rps = max(ctx)
     hid = I.make_hidden(s, BATCH * rps, SEED, "paged").cuda()
@@ -67,8 +77,8 @@ def test_paged_cache_is_bit_identical_to_sequence_major(pair):
     B = 16
     for step in range(3):
         noise = I.make_logit_noise(BATCH, B, s.vocab, SEED, f"paged.{step}").cuda()
-        a = _step(flat, BATCH, B, noise)
-        b = _step(paged, BATCH, B, noise, drafted_in=a[0])
+        a = _step(flat, s, BATCH, B, noise)
+        b = _step(paged, s, BATCH, B, noise, drafted_in=a[0])
         for x, y in zip(a, b):
             assert torch.equal(x, y)
         assert torch.equal(flat.last_token[:BATCH], paged.last_token[:BATCH])
@@ -85,8 +95,7 @@ def test_paged_cache_is_bit_identical_to_sequence_major(pair):
 
 
 def test_out_of_range_page_is_flagged(pair):
-    flat, paged, pt = pair
-    s = W_TINY.shape
+    flat, paged, pt, s = pair
     saved = pt.clone()
     paged.len[:BATCH] = torch.tensor([60, 0, 0], dtype=torch.int32, device="cuda")
     pt[0, 1] = 10_000                     # the page that positions 64..127 of sequence 0 map to

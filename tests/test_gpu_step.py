@@ -248,7 +248,7 @@ def test_options_round_trip(tiny):
     assert d.get_option(BND.OPT_CHAIN_MAX) == 8
     assert d.get_option(BND.OPT_ATTN_MODE) == 0
     for opt, bad in ((BND.OPT_WAIT_LIMIT_NS, 10), (BND.OPT_CHAIN_MAX, 9), (BND.OPT_GEMV_VARIANT, 6),
-                     (BND.OPT_ATTN_SPLIT, 17), (BND.OPT_ATTN_MODE, 3), (BND.OPT_ATTN_MODE, -1), (99, 1)):
+                     (BND.OPT_ATTN_SPLIT, 17), (BND.OPT_ATTN_MODE, 4), (BND.OPT_ATTN_MODE, -1), (99, 1)):
         with pytest.raises(BND.DFlashError):
             d.set_option(opt, bad)
     d.set_option(BND.OPT_CHAIN_MAX, 3)
