@@ -315,7 +315,10 @@ int dflash_trace_events(dflash_handle* h, void* const* events, int32_t n_events)
  *       2 standalone attention, 3 block embedding, 4 verification)   [1] SM id
  *   [2] entry   [3] set-up done
  *   [4+4p] phase p started   [5+4p] its input ready   [6+4p] first operand landed
- *   [7+4p] phase p finished (p < 8; other kernels fill [5] and a few of [6..9] only)
+ *   [7+4p] phase p finished (p < 8; other kernels fill [5] and a few of [6..9] only;
+ *   the tensor-core flat attention kernel also [10] ns its producer waited for a free
+ *   stage, [11] ns its MMA issuer had nothing to issue, [12] and [13] ns its softmax rows
+ *   waited for scores and for the previous PV, [14] its key steps)
  *   [36] exit
  * Unset stamps keep whatever the buffer held, so clear it first. Calling this again
  * restarts at record 0. Stamps cost a few instructions per CTA. */
