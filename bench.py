@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--trace-steps", type=int, default=10)
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the block-size draft sweep and the fused target-verify measurement")
+    ap.add_argument("--attn-mode", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="attention kernel (DFLASH_OPT_ATTN_MODE): 0 chosen by shape, 1 clusters, "
+                         "2 flat split on the tensor cores where the shape allows, 3 flat on mma.sync")
     return ap.parse_args()
 
 
@@ -428,6 +431,7 @@ def run_cuda(a):
     ctx_max = int(ctx_lens.max())
     cap = ctx_max + (a.warmup + a.steps + a.trace_steps + 4) * B + B
     dr = BND.Drafter(s, weights, max_block=B, max_batch=batch, kv_capacity=cap)
+    dr.set_option(BND.OPT_ATTN_MODE, a.attn_mode)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     log(f"[bench] weights ready in {time.time() - t_setup:.1f}s; prefill {ctx_max} positions x {batch}")
@@ -831,6 +835,7 @@ def run_cuda(a):
             "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden states and logits)",
             "config": workload_config(w, ws, a.seed),
             "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
+            "attn_mode": a.attn_mode,
             "drafted_tok_per_s": value * (B - 1), "committed_tok_per_s": value * mean_tau, "mean_tau": mean_tau,
             "draft_ms": draft_ms, "draft_ms_by_block": draft_by_block, "fused_target_verify": fused,
             "prefill": prefill,
