@@ -13,7 +13,8 @@
 // Per step (32 keys of both heads; K and V fp16, staged by TMA in boxes of 32 positions with
 // the 128-byte swizzle, the two heads' keys stacked into 64-key operands; a 4-deep ring):
 //   S  = Q Kᵀ  : tcgen05.mma kind::f16, M = 128, N = 64 keys, K = 128 dims; fp32 in TMEM
-//                (two buffers). Row r only uses its own head's 32 columns.
+//                (three buffers: the issuer runs two steps ahead). Row r only uses its own
+//                head's 32 columns.
 //   softmax    : four warps, one query row per thread: the row's 32 scores from TMEM, the
 //                running max (log2 units) and sum, P = exp2(S - m) as fp16 into shared
 //                memory (two buffers), where the other head's 32 columns of the row stay zero.
@@ -24,8 +25,8 @@
 //                when the tile max exceeds it by more than 8 (log2 units; P then stays
 //                <= 256, exact enough in fp16); then that row of O in TMEM and its sum are
 //                scaled by exp2(old - new), after the PVs issued so far have completed.
-// Roles: warps 0-3 softmax/output, warp 4 lane 0 MMA issuer (one QKᵀ ahead of the PV of the
-// same segment), warp 5 lane 0 TMA producer. Every wait is bounded, none waits for a phase
+// Roles: warps 0-3 softmax/output, warp 4 lane 0 MMA issuer (up to two QKᵀ ahead of the PVs
+// within a segment), warp 5 lane 0 TMA producer. Every wait is bounded, none waits for a phase
 // older than the last its barrier can have completed, and the softmax warps take every wait
 // and every exit together (warp-collective TMEM accesses never diverge).
 #include "internal.h"
@@ -48,12 +49,13 @@ constexpr int Q_OFF = 0;                  // 128 rows x 128 dims fp16: two 64-di
 constexpr int P_OFF = 32768;              // two buffers of 128 rows x 64 keys fp16 (16 KB each)
 constexpr int RING_OFF = 65536;           // TST x (K box 0, K box 1, V box 0, V box 1)
 constexpr int BAR_OFF = RING_OFF + TST * TTILE;
-// mbarriers: full[TST], empty[TST], sready[2], sfree[2], pready[2], pvready[2], qready, mdone
-constexpr int NBARS = 2 * TST + 10;
+// mbarriers: full[TST], empty[TST], sready[NS], sfree[NS], pready[2], pvready[2], qready, mdone
+constexpr int NS = 3;  // S buffers in TMEM
+constexpr int NBARS = 2 * TST + 2 * NS + 6;
 constexpr int FLAG_OFF = BAR_OFF + NBARS * 8;     // [0] abort, [1] merging, [2] sharers, [3] rank, [4] tmem base
 constexpr int CS_OFF = FLAG_OFF + 32;             // merge: contributor slots [kMaxCtas]
 constexpr int PRE_OFF = CS_OFF + kMaxCtas * 4;    // tiles per head before each sequence [batch + 1]
-constexpr uint32_t S_COL = 0, O_COL = 128;        // TMEM columns: S buffers at 0, 64; O at 128
+constexpr uint32_t S_COL = 0, O_COL = 256;        // TMEM columns: S buffers at 0, 64, 128; O at 256
 constexpr float kRescale = 8.f;                   // log2 growth of a row max that moves its reference
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, A K-major, B K-major
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
   uint64_t* full = bars;
   uint64_t* empty = bars + TST;
   uint64_t* sready = bars + 2 * TST;
-  uint64_t* sfree = sready + 2;
-  uint64_t* pready = sfree + 2;
+  uint64_t* sfree = sready + NS;
+  uint64_t* pready = sfree + NS;
   uint64_t* pvready = pready + 2;
   uint64_t* qready = pvready + 2;
   uint64_t* mdone = qready + 1;
@@ -154,9 +156,11 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NS; ++b) {
       mbar_init(&sready[b], 1);
       mbar_init(&sfree[b], TR);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&pready[b], TR);
       mbar_init(&pvready[b], 1);
     }
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
     }
     fence_async_shared();
   }
-  if (warp == 4) tmem_alloc(reinterpret_cast<uint32_t*>(smem + FLAG_OFF + 16), 256);
+  if (warp == 4) tmem_alloc(reinterpret_cast<uint32_t*>(smem + FLAG_OFF + 16), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -290,8 +294,8 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
     pdl_wait();
     pdl_launch_dependents();
     if (lane == 0) {
-      auto qk = [&](int i) {  // S[i % 2] = Q [K of both heads]ᵀ (its inputs are ready)
-        const int st = i % TST, b = i & 1;
+      auto qk = [&](int i) {  // S[i % NS] = Q [K of both heads]ᵀ (its inputs are ready)
+        const int st = i % TST, b = i % NS;
         tc_fence_after();
         const uint32_t q0 = smem_u32(smem + Q_OFF), k0 = smem_u32(smem + RING_OFF + st * TTILE);
 #pragma unroll
@@ -321,18 +325,18 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
       Cursor q{0, 0, 0, 1};
       if (n > 0) locate(T0, q.s, q.g2, q.t, q.nt);
       int nqk = 0, npv = 0, seg = -1;
-      bool first_of[2] = {false, false};
+      bool first_of[NS] = {false, false, false};
       uint64_t t_idle = globaltimer_ns();
       uint64_t t_idle_sum = 0, t_prev = globaltimer_ns();  // timeline: time with nothing to issue
       while (npv < n) {
         bool moved = false;
-        if (nqk < n && nqk <= npv + 1) {
+        if (nqk < n && nqk <= npv + (NS - 1)) {
           const bool start = nqk == 0 || q.t == 0;
           if (mbar_try_wait(&full[nqk % TST], (nqk / TST) & 1) &&
-              (nqk < 2 || mbar_try_wait(&sfree[nqk & 1], ((nqk >> 1) - 1) & 1)) &&
+              (nqk < NS || mbar_try_wait(&sfree[nqk % NS], ((nqk / NS) - 1) & 1)) &&
               (!start || mbar_try_wait(qready, (seg + 1) & 1))) {
             qk(nqk);
-            first_of[nqk & 1] = start;
+            first_of[nqk % NS] = start;
             if (start) ++seg;
             if (nqk + 1 < n) advance(q);
             ++nqk;
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
           }
         }
         if (npv < nqk && mbar_try_wait(&pready[npv & 1], (npv >> 1) & 1)) {
-          pv(npv, first_of[npv & 1]);
+          pv(npv, first_of[npv % NS]);
           ++npv;
           moved = true;
         }
@@ -410,9 +414,9 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
       }
       float m = -INFINITY, l = 0.f;  // reference max (log2 units) and the row sum against it
       for (int i = j; i < j + seg && ok; ++i) {
-        const int b = i & 1;
+        const int b = i & 1, sb = i % NS;
         const uint64_t tw0 = (tl && r == 0) ? globaltimer_ns() : 0;
-        if (!wait(&sready[b], (i >> 1) & 1)) break;
+        if (!wait(&sready[sb], (i / NS) & 1)) break;
         if (tl && r == 0) t_ws += globaltimer_ns() - tw0;
         if (i == 0 && r == 0) tl_stamp(tl, 6);
         tc_fence_after();
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
           uint32_t u[TKT / 16][16];
 #pragma unroll
           for (int c16 = 0; c16 < TKT / 16; ++c16)
-            tmem_ld16_nw(tmem + lane_base + S_COL + b * (2 * TKT) + hh * TKT + c16 * 16, u[c16]);
+            tmem_ld16_nw(tmem + lane_base + S_COL + sb * (2 * TKT) + hh * TKT + c16 * 16, u[c16]);
           tmem_wait_ld();
 #pragma unroll
           for (int c16 = 0; c16 < TKT / 16; ++c16)
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
             for (int k = 0; k < 16; ++k) sc[c16 * 16 + k] = __uint_as_float(u[c16][k]);
         }
         tc_fence_before();
-        mbar_arrive(&sfree[b]);
+        mbar_arrive(&sfree[sb]);
         const int key0 = (ta + i - j) * TKT;
         float mx = -INFINITY;
 #pragma unroll
@@ -679,7 +683,7 @@ __global__ void __launch_bounds__(192, 1) attn_flat_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 256);
+  if (warp == 4) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0) tl_stamp(tl, kTlExit);
 }
 
