@@ -757,6 +757,11 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
           const int ca = cta_of_unit(static_cast<uint32_t>(t) * P.KB, U, Gp);
           const int cb = cta_of_unit(static_cast<uint32_t>(t + 1) * P.KB - 1, U, Gp);
           const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::NCOL;
+          // The CTA whose last tile this is finishes it alone (keeping its own sum in TMEM)
+          // with one row group, and with several when one other CTA shares the tile and
+          // runs past its end (no CTA lies wholly inside it): then nobody else finishes.
+          const bool solo = c == ca && (NB == 1 || (C::MINB == 1 && cb == ca + 1 &&
+                                                     unit_begin(cb + 1, U, Gp) > static_cast<uint32_t>(t + 1) * P.KB));
           if (ca == cb) {
             for (int ch = 0; ch < NB; ++ch) {
               float v[16], w[16];
@@ -769,7 +774,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               to_rows<C::XLD>(v, m, e, xch, w);
               epilogue_rows<NB>(P, t, ch, w, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
-          } else if (c != ca || NB > 1) {
+          } else if (!solo) {
             // split tile, contributor (with several row groups, every CTA of the tile): its
             // partial goes to its slot ([ROWS][128] fp32, row layout), then it is counted in
             const int slot = part_slot(c, t, U, Gp, P.KB);
@@ -836,13 +841,13 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               }
             }
           } else {
-            // split tile of a single-row-group pass, finisher: CTA ca, whose last tile this is.
-            // The others reach it first (cb) or only (CTAs in between), so ca is usually the
-            // last to get here; it keeps its own sum, waits for the cb - ca other partials and
-            // adds them in CTA order.
+            // split tile, sole finisher: CTA ca, whose last tile this is. The others reach it
+            // first (cb) or only (CTAs in between), so ca is usually the last to get here; it
+            // keeps its own sum, waits for the cb - ca other partials and adds them in CTA
+            // order.
             const RowPos rp = row_pos(e);
             float own[16];
-            if (NB == 1) {  // own accumulator out of TMEM while the others finish
+            if constexpr (NB == 1) {  // own accumulator out of TMEM while the others finish
               float v[16];
               tmem_ld_acc(taddr, 0, split, v);
               tc_fence_before();
@@ -866,38 +871,58 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             }
             // the poller's ld.acquire.gpu plus the CTA barrier order the partial loads after
             // the contributors' releases
-            for (int ch = 0; ch < NB; ++ch) {
-              if (ch > 0) epilogue_prefetch<NB, C::MINB>(P, t, ch, e, s_pos, pre);
-              // the others' partials, up to PR CTAs' loads in flight per round; the first
-              // round is issued before this CTA's own sum is read out
-              constexpr int PR = C::MINB == 1 ? 8 : 4;
-              auto part_row = [&](int cc) {
-                return P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128 +
-                       (ch * 16 + rp.r) * 128 + rp.c0;
-              };
-              float a[PR][16];
+            if constexpr (NB > 1) {
+              // one other partial (cb = ca + 1), its rows loaded AH chunks ahead of the chunk
+              // being finished so that the chunks' global round trips overlap
+              const float* pb = P.part + static_cast<size_t>(part_slot(cb, t, U, Gp, P.KB)) * C::ROWS * 128 +
+                                rp.r * 128 + rp.c0;
+              constexpr int AH = NB >= 8 ? 2 : 1;  // chunks loaded ahead (registers allowing)
+              float a0[16], a1[16];
+              ld16(pb, a0);
+              if (AH == 2) ld16(pb + 16 * 128, a1);
+              for (int ch = 0; ch < NB; ++ch) {
+                float a2[16];
+                if (ch + AH < NB) {
+                  ld16(pb + (ch + AH) * 16 * 128, a2);
+                } else {
 #pragma unroll
-              for (int q2 = 0; q2 < PR; ++q2)
-                if (ca + 1 + q2 <= cb) ld16(part_row(ca + 1 + q2), a[q2]);
-              float v[16];
-              if (NB == 1) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = own[k];
-              } else {
-                float a0[16];
-                tmem_ld_acc(taddr, ch, split, a0);
+                  for (int k = 0; k < 16; ++k) a2[k] = 0.f;
+                }
+                if (ch > 0) epilogue_prefetch<NB, C::MINB>(P, t, ch, e, s_pos, pre);
+                float a0t[16], v[16];
+                tmem_ld_acc(taddr, ch, split, a0t);
                 if (ch == NB - 1) {
                   tc_fence_before();
                   mbar_arrive(&tempty[acc]);
                 }
-                to_rows<C::XLD>(a0, m, e, xch, v);
-              }
-              for (int cc0 = ca + 1; cc0 <= cb; cc0 += PR) {
-                if (cc0 > ca + 1) {
+                to_rows<C::XLD>(a0t, m, e, xch, v);
 #pragma unroll
-                  for (int q2 = 0; q2 < PR; ++q2)
-                    if (cc0 + q2 <= cb) ld16(part_row(cc0 + q2), a[q2]);
+                for (int k = 0; k < 16; ++k) v[k] += a0[k];
+                epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  if (AH == 2) {
+                    a0[k] = a1[k];
+                    a1[k] = a2[k];
+                  } else {
+                    a0[k] = a2[k];
+                  }
                 }
+              }
+            } else {
+              // one row group: the others' partials, up to PR CTAs' loads in flight per round
+              constexpr int PR = C::MINB == 1 ? 8 : 4;
+              auto part_row = [&](int cc) {
+                return P.part + static_cast<size_t>(part_slot(cc, t, U, Gp, P.KB)) * C::ROWS * 128 + rp.r * 128 + rp.c0;
+              };
+              float v[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[k] = own[k];
+              for (int cc0 = ca + 1; cc0 <= cb; cc0 += PR) {
+                float a[PR][16];
+#pragma unroll
+                for (int q2 = 0; q2 < PR; ++q2)
+                  if (cc0 + q2 <= cb) ld16(part_row(cc0 + q2), a[q2]);
 #pragma unroll
                 for (int q2 = 0; q2 < PR; ++q2)
                   if (cc0 + q2 <= cb) {
@@ -905,7 +930,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
                     for (int k = 0; k < 16; ++k) v[k] += a[q2][k];
                   }
               }
-              epilogue_rows<NB>(P, t, ch, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
+              epilogue_rows<NB>(P, t, 0, v, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
           }
         }
