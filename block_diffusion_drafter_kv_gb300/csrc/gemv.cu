@@ -462,6 +462,42 @@ DEV void phase_units(const GemvParams& P, int c, int G, uint32_t& U, uint32_t& u
   }
 }
 
+// Order in which CTA c visits the tiles of its unit range [u0, u1): ascending, except that in
+// passes of several row groups (an epilogue of many 16-row chunks) a last tile shared with
+// exactly one other CTA (c + 1, whose first tile it is and whose range runs past it) comes
+// second when one whole tile lies between. c finishes that tile, and c + 1's part of it is the
+// first work c + 1 does, so c can finish it while the whole tile streams: at the end of the
+// phase only that tile's epilogue remains, not two tiles' work. (The whole tile and the moved
+// one use different accumulators, so the MMAs never wait for the finishing. With more whole
+// tiles, or a one-chunk epilogue, the move measured slower.)
+struct TileOrder {
+  uint32_t u0, u1;
+  int ta, tb;
+  bool swap;
+  DEV int count() const { return u0 < u1 ? tb - ta + 1 : 0; }
+  DEV int tile(int j) const { return !swap ? ta + j : j == 0 ? ta : j == 1 ? tb : ta + j - 1; }
+};
+template <int NB>
+DEV TileOrder tile_order(uint32_t u0, uint32_t u1, uint32_t U, int Gp, int c, uint32_t KB) {
+  TileOrder o{u0, u1, 0, -1, false};
+  if (u0 >= u1) return o;
+  o.ta = static_cast<int>(u0 / KB);
+  o.tb = static_cast<int>((u1 - 1) / KB);
+  const uint32_t tb_end = static_cast<uint32_t>(o.tb + 1) * KB;
+  o.swap = NB > 1 && o.tb - o.ta == 2 && u1 < tb_end && c + 1 < Gp && cta_of_unit(tb_end - 1, U, Gp) == c + 1 &&
+           unit_begin(c + 2, U, Gp) > tb_end;
+  return o;
+}
+// The k-th unit of the range in visiting order (ascending within a tile).
+DEV uint32_t unit_at(const TileOrder& o, uint32_t KB, uint32_t k) {
+  if (!o.swap) return o.u0 + k;
+  const uint32_t e0 = static_cast<uint32_t>(o.ta + 1) * KB, b1 = static_cast<uint32_t>(o.tb) * KB;
+  const uint32_t n0 = e0 - o.u0, n1 = o.u1 - b1;
+  if (k < n0) return o.u0 + k;
+  if (k < n0 + n1) return b1 + (k - n0);
+  return e0 + (k - n0 - n1);
+}
+
 // A chain of projection phases in one persistent launch. Phase p+1 reads what phase p
 // wrote, so its activation tiles are loaded only after the phase-p grid barrier, but its
 // weight tiles are streamed into every free ring stage before that barrier.
@@ -544,6 +580,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         uint32_t U, u0, u1;
         int Gp;
         phase_units(P, c, G, U, u0, u1, Gp);
+        const TileOrder ord = tile_order<NB>(u0, u1, U, Gp, c, P.KB);
         const uint32_t n = u1 > u0 ? u1 - u0 : 0;
         const uint32_t pre = n < static_cast<uint32_t>(C::STAGES) ? n : C::STAGES;
         const uint32_t stage_bytes = C::A_BYTES + (P.b_lo ? 2 : 1) * C::KS * C::B_PLANE;
@@ -556,7 +593,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             ok = false;
             break;
           }
-          const uint32_t u = u0 + a_only;
+          const uint32_t u = unit_at(ord, P.KB, a_only);
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
         }
@@ -574,7 +611,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         // activations of the stages armed above (issued even after a failed wait so that
         // every armed stage completes and the drain below cannot stall)
         for (uint32_t k = 0; k < a_only; ++k) {
-          const uint32_t u = u0 + k, s = (it + k) % C::STAGES;
+          const uint32_t u = unit_at(ord, P.KB, k), s = (it + k) % C::STAGES;
           load_b<C::KS, C::B_SUB, C::B_PLANE>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
         }
         it += a_only;
@@ -588,7 +625,7 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
             ok = false;
             break;
           }
-          const uint32_t u = u0 + k;
+          const uint32_t u = unit_at(ord, P.KB, k);
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           load_a<C::KS>(P, u / P.KB, u % P.KB, sA + s * C::A_BYTES, &full[s], pol_w);
           load_b<C::KS, C::B_SUB, C::B_PLANE>(P, u % P.KB, sB + s * C::B_BYTES, &full[s], pol_x);
@@ -616,7 +653,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         int Gp;
         phase_units(P, c, G, U, u0, u1, Gp);
         if (u0 >= u1) continue;
-        for (int t = static_cast<int>(u0 / P.KB); ok && static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+        const TileOrder ord = tile_order<NB>(u0, u1, U, Gp, c, P.KB);
+        for (int jt = 0; ok && jt < ord.count(); ++jt, ++lt) {
+          const int t = ord.tile(jt);
           const uint32_t ub = max(u0, static_cast<uint32_t>(t) * P.KB);
           const uint32_t ue = min(u1, static_cast<uint32_t>(t + 1) * P.KB);
           const int acc = lt & 1;
@@ -742,7 +781,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
         }
       };
       if (u0 < u1) {
-        for (int t = static_cast<int>(u0 / P.KB); static_cast<uint32_t>(t) * P.KB < u1; ++t, ++lt) {
+        const TileOrder ord = tile_order<NB>(u0, u1, U, Gp, c, P.KB);
+        for (int jt = 0; jt < ord.count(); ++jt, ++lt) {
+          const int t = ord.tile(jt);
           const int acc = lt & 1;
           EpiPre pre;
           epilogue_prefetch<NB, C::MINB>(P, t, 0, e, s_pos, pre);
