@@ -816,8 +816,9 @@ __global__ void __launch_bounds__(192, C::MINB) gemv_kernel(const __grid_constan
               epilogue_rows<NB>(P, t, ch, w, e, s_inv, s_bv, s_bi, s_pos, s_seq, pre);
             }
           } else if (!solo) {
-            // split tile, contributor (with several row groups, every CTA of the tile): its
-            // partial goes to its slot ([ROWS][128] fp32, row layout), then it is counted in
+            // split tile, contributor (with several row groups, every CTA of the tile unless
+            // the tile has a sole finisher): its partial goes to its slot ([ROWS][128] fp32,
+            // row layout), then it is counted in
             const int slot = part_slot(c, t, U, Gp, P.KB);
             float* dst = P.part + static_cast<size_t>(slot) * C::ROWS * 128;
             const RowPos rp = row_pos(e);
