@@ -176,14 +176,26 @@ class Drafter:
 
     # -- the three calls of the step ---------------------------------------------------
     def inject(self, hidden, rows_per_seq: int, n_new, batch: int, stream=None):
+        import torch
+        _require(hidden, torch.bfloat16, "hidden")
+        _require(n_new, torch.int32, "n_new")
         check(self.L.dflash_inject_ctx(self.h, hidden.data_ptr(), rows_per_seq, n_new.data_ptr(), batch,
                                        _stream(stream)), "dflash_inject_ctx")
 
     def draft(self, batch: int, block: int, drafted, logits=None, x_trace=None, stream=None):
+        import torch
+        _require_opt(drafted, torch.int32, "drafted")
+        _require_opt(logits, torch.float32, "logits")
+        _require_opt(x_trace, torch.float32, "x_trace")
         check(self.L.dflash_draft_block(self.h, batch, block, _ptr(drafted), _ptr(logits), _ptr(x_trace),
                                         _stream(stream)), "dflash_draft_block")
 
     def verify(self, target_logits, drafted, batch: int, block: int, accept_len, committed, stream=None):
+        import torch
+        _require(target_logits, torch.float32, "target_logits")
+        _require_opt(drafted, torch.int32, "drafted")
+        _require(accept_len, torch.int32, "accept_len")
+        _require(committed, torch.int32, "committed")
         check(self.L.dflash_verify_greedy(self.h, target_logits.data_ptr(), _ptr(drafted), batch, block,
                                           accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
               "dflash_verify_greedy")
@@ -192,6 +204,12 @@ class Drafter:
                         accept_len, committed, stream=None):
         """Speculative-sampling verification at `temperature` with caller-drawn uniforms
         (fp32 [batch][B]: accept tests, then the sampling draw)."""
+        import torch
+        _require(target_logits, torch.float32, "target_logits")
+        _require_opt(drafted, torch.int32, "drafted")
+        _require(uniforms, torch.float32, "uniforms")
+        _require(accept_len, torch.int32, "accept_len")
+        _require(committed, torch.int32, "committed")
         check(self.L.dflash_verify_sampling(self.h, target_logits.data_ptr(), _ptr(drafted), uniforms.data_ptr(),
                                             float(temperature), batch, block, accept_len.data_ptr(),
                                             committed.data_ptr(), _stream(stream)), "dflash_verify_sampling")
@@ -200,6 +218,12 @@ class Drafter:
                       committed, stream=None):
         """Greedy verification from the target's last hidden states (bf16 [batch*B][Ht]), its
         final-norm gain (bf16 [Ht]) and LM head (bf16 [V][Ht])."""
+        import torch
+        for t, n in ((target_hidden, "target_hidden"), (target_gain, "target_gain"), (target_lm_head, "target_lm_head")):
+            _require(t, torch.bfloat16, n)
+        _require_opt(drafted, torch.int32, "drafted")
+        _require(accept_len, torch.int32, "accept_len")
+        _require(committed, torch.int32, "committed")
         check(self.L.dflash_verify_greedy_hidden(self.h, target_hidden.data_ptr(), target_gain.data_ptr(),
                                                  target_lm_head.data_ptr(), _ptr(drafted), batch, block,
                                                  accept_len.data_ptr(), committed.data_ptr(), _stream(stream)),
@@ -207,6 +231,10 @@ class Drafter:
 
     # -- helpers -------------------------------------------------------------------------
     def linear(self, W, X, Y, stream=None):
+        import torch
+        _require(W, torch.bfloat16, "W")
+        _require(X, torch.bfloat16, "X")
+        _require(Y, torch.float32, "Y")
         check(self.L.dflash_linear_bf16(self.h, W.data_ptr(), W.shape[0], W.shape[1], X.data_ptr(), X.shape[0],
                                         Y.data_ptr(), _stream(stream)), "dflash_linear_bf16")
 
@@ -264,6 +292,11 @@ def _require(t, dtype, name):
     if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
         raise DFlashError(DFLASH_E_INVAL, f"{name} must be a contiguous {dtype} CUDA tensor "
                                           f"(got {t.dtype}, cuda={t.is_cuda}, contiguous={t.is_contiguous()})")
+
+
+def _require_opt(t, dtype, name):
+    if t is not None:
+        _require(t, dtype, name)
 
 
 def verify_greedy_noalloc(target_logits, drafted, batch: int, block: int, accept_len, committed, last_token,

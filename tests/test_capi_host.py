@@ -122,3 +122,27 @@ def test_options_and_error_read_need_a_handle(L):
     assert L.dflash_selftest_timeout(None, None) == -1
     f = ctypes.c_int32(0)
     assert L.dflash_read_device_error(None, ctypes.byref(f), 0, None) == -1
+
+
+def test_wrappers_refuse_tensors_the_library_would_misread():
+    """The binding checks dtype, device and contiguity before any library call: a handle
+    that was never created (no library, no GPU) is enough to see each refusal."""
+    import torch
+    d = object.__new__(B.Drafter)   # no handle: reaching the library would raise AttributeError
+    f32 = torch.zeros(2, 16, 8)
+    i32 = torch.zeros(2, 16, dtype=torch.int32)
+    bf = torch.zeros(5, 32, 64, dtype=torch.bfloat16)
+    calls = [
+        lambda: d.inject(bf, 16, torch.zeros(2, dtype=torch.int32), 2),            # CPU tensors
+        lambda: d.inject(bf.float(), 16, torch.zeros(2, dtype=torch.int32), 2),    # fp32 hidden
+        lambda: d.draft(2, 16, i32.to(torch.int64)),                               # int64 drafted
+        lambda: d.draft(2, 16, i32, logits=f32.transpose(1, 2)),                   # non-contiguous logits
+        lambda: d.verify(f32.double(), i32, 2, 16, i32[:, 0], i32),                # fp64 logits
+        lambda: d.verify_sampling(f32, i32, f32[:, :, 0].half(), 1.0, 2, 16, i32[:, 0], i32),
+        lambda: d.verify_hidden(bf, bf, bf.float(), i32, 2, 16, i32[:, 0], i32),
+        lambda: d.linear(bf[0], bf[0], bf[0]),                                     # bf16 output
+    ]
+    for call in calls:
+        with pytest.raises(B.DFlashError) as ei:
+            call()
+        assert ei.value.status == B.DFLASH_E_INVAL
