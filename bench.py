@@ -172,7 +172,7 @@ def step_bytes_flops(s, batch, B, n_ctx, tau):
 
 class NvmlClockSampler:
     """SM clock, power and clock-event reasons of this process's GPU, read through NVML
-    (the driver's management library, loaded with ctypes) every `period_ms` from a thread.
+    (NVIDIA's management library, loaded with ctypes) every `period_ms` from a thread.
     Only reads; changes no setting. Raises in __init__ when NVML is not usable."""
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
